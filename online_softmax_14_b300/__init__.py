@@ -1,0 +1,22 @@
+"""Exact softmax attention (online-softmax forward, recompute backward) for B300.
+
+The compute runs in hand-written sm_103a CUDA kernels behind the C-ABI library
+``libfa.so`` (declared in ``include/fa.h``).  This package is the thin Python
+binding over that library: it marshals tensor pointers, sizes and the current
+CUDA stream, and nothing else.  ``online_softmax_14_b300.inputs`` (the seeded
+input generator) imports without the library; every other name loads it on first
+use and raises if it has not been built.
+"""
+
+_BINDING_NAMES = None
+
+
+def __getattr__(name):
+    if name.startswith("__"):
+        raise AttributeError(name)
+    from . import _binding
+
+    try:
+        return getattr(_binding, name)
+    except AttributeError:
+        raise AttributeError(f"module 'online_softmax_14_b300' has no attribute {name!r}") from None
