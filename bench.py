@@ -1,0 +1,347 @@
+"""Benchmark of the attention forward on B300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fa|reference]
+
+A step is one fa_fwd call over the whole batch of the workload (default: bf16,
+causal, B=2 H=32 N=8192 d=128, the long-sequence throughput case).  The metric
+is attention-forward TFLOP/s counting 4*B*H*N^2*d multiply-add FLOPs, halved for
+causal masking, with inputs resident in device memory; the inputs (3 x 134 MB)
+exceed the 126 MB L2, so no L2 flush is needed between steps.  The line also
+carries:
+  * roofline  -- achieved TFLOP/s of the kernel against the measured dense-bf16
+                 tensor peak (MEASURED_PEAKS.json), with DRAM traffic per launch
+                 from an ncu capture of the same kernel sources (null otherwise);
+  * e2e       -- the same metric through the public API with the inputs copied
+                 from pinned host memory and O, lse copied back inside each step;
+  * cpu_baseline -- the float64 CPU oracle timed on a bounded sample (rank 0, N=1);
+  * clocks    -- SM clocks and throttle reasons sampled during the timed region.
+With --impl reference the float64 oracle itself is timed (rank 0 only).
+Multi-GPU (torchrun): every rank runs its own replica of the workload, no data
+exchange; value = all ranks' FLOPs / the slowest rank's time ("weak" scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from online_softmax_14_b300.inputs import WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s at bf16 (causal halved) and % of B300 dense-BF16 peak"
+DEFAULT_WORKLOAD = "bf16_causal_B2_H32_N8192_d128"
+FALLBACK_BF16_TFLOPS = 1800.0  # used only when MEASURED_PEAKS.json is absent
+
+# DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture,
+# valid only for the kernel sources whose digest is recorded with it.
+NCU_TRAFFIC = {}  # {workload: {"bytes": int, "src_digest": str}}
+
+
+def flops_per_step(w) -> float:
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    return f / 2 if w.causal else f
+
+
+def kernel_src_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "online_softmax_14_b300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """Samples SM clock and throttle reasons with NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self.period = period_s
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            props = torch.cuda.get_device_properties(device_index)
+            bus = getattr(props, "pci_bus_id", None)
+            if bus is not None:
+                pci = f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(pci)
+            else:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # NVML unavailable: report that instead of clocks
+            self.err = repr(e)
+
+    def _run(self):
+        nv = self.nv
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = get_reasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "err", "")}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_heads(w, inputs, heads, causal):
+    import oracle
+
+    t0 = time.perf_counter()
+    for (b, h) in heads:
+        sl = slice(b, b + 1)
+        kl = None if inputs["kv_len"] is None else [int(inputs["kv_len"][b])]
+        oracle.attention_fwd(inputs["q"][sl, h:h + 1], inputs["k"][sl, h:h + 1], inputs["v"][sl, h:h + 1],
+                             inputs["scale"], causal=causal, kv_len=kl)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, inputs, budget_s=15.0):
+    """The oracle, as it stands, on whole heads of the workload until ~budget_s."""
+    per_head = flops_per_step(w) / (w.B * w.H)
+    heads, t = [], 0.0
+    i = 0
+    while t < budget_s and i < w.B * w.H:
+        bh = (i * 7) % (w.B * w.H)
+        t += oracle_heads(w, inputs, [(bh // w.H, bh % w.H)], w.causal)
+        heads.append(bh)
+        i += 1
+    return {"value": per_head * len(heads) / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{len(heads)} whole (b,h) heads of {w.name} ({t:.1f} s, float64 NumPy, full N x N scores)"}
+
+
+# ------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import online_softmax_14_b300 as fa
+
+    inputs = make_workload(w, seed=args.seed + rank)
+    dev = torch.device("cuda", local)
+    q, k, v = (inputs[n].to(dev) for n in ("q", "k", "v"))
+    kv = None if inputs["kv_len"] is None else inputs["kv_len"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dt = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP32
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_fwd_ex(dt, q, k, v, o, lse, kv, w.B, w.H, w.N, w.d, inputs["scale"], w.causal, stream)
+
+    for _ in range(args.warmup):
+        step()
+    fa.fa_check_device_error(stream)
+
+    clk = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    fa.fa_check_device_error(stream)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    f_step = flops_per_step(w)
+    value = f_step * world / (ms_max * 1e-3) / 1e12
+    achieved = f_step / (ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> kernel -> host outputs
+    hq, hk, hv = (inputs[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    if kv is not None:
+        hkv = inputs["kv_len"].pin_memory()
+        h2d += hkv.numel() * hkv.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        if kv is not None:
+            kv.copy_(hkv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error(stream)
+    ms_e2e = e2.elapsed_time(e3) / args.e2e_steps
+    if dist:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_value = f_step * world / (ms_e2e * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    digest = kernel_src_digest()
+    tr = NCU_TRAFFIC.get(w.name)
+    traffic = tr["bytes"] if tr and tr["src_digest"] == digest else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1), see online_softmax_14_b300/inputs.py)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "seed": args.seed, "inputs_exceed_l2": True, "l2_flush": False,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "src_digest": digest},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, w, rank, world):
+    """The float64 CPU oracle on the host cores, one whole (b, h) head per step."""
+    if rank != 0:
+        return
+    inputs = make_workload(w, seed=args.seed)
+    heads = [((i * 7) % (w.B * w.H)) for i in range(args.warmup + args.steps)]
+    heads = [(bh // w.H, bh % w.H) for bh in heads]
+    for hh in heads[: args.warmup]:
+        oracle_heads(w, inputs, [hh], w.causal)
+    t = oracle_heads(w, inputs, heads[args.warmup:], w.causal)
+    per_head = flops_per_step(w) / (w.B * w.H)
+    value = per_head * args.steps / t / 1e12
+    cores = blas_threads()
+    sample = f"one whole (b,h) head of {w.name} per step, float64 NumPy with the full N x N scores"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,114 @@
+/*
+ * fa.h -- C ABI of libfa: exact softmax attention on NVIDIA B300 (sm_103a).
+ *
+ * The operation (per batch b and head h, matrices row-major, head dim innermost):
+ *
+ *     S = scale * Q K^T,  masked entries -> -inf,
+ *     O = softmax_rows(S) V,   lse_i = ln sum_j exp(S_ij),
+ *     a row with no visible key gives O_i = 0 and lse_i = -inf.
+ *
+ * Sources: "Foundations -- Flash attention and efficient attention", sections 4
+ * (the N x N score matrix Q K^T), 7-8 (softmax with the max subtracted) and 9 (the
+ * 1/sqrt(d_k) score scale); "The Flash Attention" page, online recurrence panel
+ * (the tiled one-pass algorithm the kernels use); "Flash attention and efficient
+ * attention: Worked examples", Cell D (causal: query i sees keys j <= i) and Cell
+ * D2 (l = 0: return the zero vector).  Key padding (keys j >= kv_len[b] masked)
+ * is an extension the pages do not describe; it uses the same -inf mask.
+ *
+ * Conventions for every entry point below:
+ *   - Tensors are dense, contiguous [B, H, N, d] (d innermost); lse is [B, H, N]
+ *     float32.  All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or retains them.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream).  A returned FA_OK means the work was validated
+ *     and enqueued; kernel-side failures are reported by fa_check_device_error.
+ *   - The library never aborts the process, never calls exit and never traps.
+ *     Invalid arguments return FA_ERR_INVALID or FA_ERR_UNSUPPORTED before any
+ *     work is enqueued; fa_last_error_string() then describes the problem.
+ *   - scale must be finite and > 0 (the pages' scale is 1/sqrt(d_k)).
+ *   - Every kernel waits on its pipeline with a time limit; a wait that runs out
+ *     ends the kernel early with garbage outputs and records FA_ERR_TIMEOUT, so
+ *     a broken pipeline cannot hang the GPU.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,     /* bad pointer, size, alignment or scale */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not served (head dim, device) */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 4      /* a kernel's bounded pipeline wait ran out */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+/*
+ * fa_fwd -- attention forward, bfloat16 inputs and output, float32 lse.
+ *   q, k, v : const bf16*, [B, H, N, d], 16-byte aligned.
+ *   o       : bf16*, [B, H, N, d], 16-byte aligned; written.
+ *   lse     : float*, [B, H, N] or NULL (then not written); natural-log
+ *             log-sum-exp of each row's scaled, masked scores.
+ *   d       : 64 or 128 (else FA_ERR_UNSUPPORTED).
+ *   causal  : nonzero -> query i attends to keys j <= i.
+ * Runs on the tensor cores (tcgen05.mma, accumulators in tensor memory,
+ * operands staged by TMA); the N x N scores never reach device memory.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_ex -- as fa_fwd, with the element type and key padding explicit.
+ *   dtype  : FA_BF16 (tensor cores; d in {64, 128}) or FA_FP32 (float32 in and
+ *            out on the CUDA cores; 1 <= d <= 128; q, k, v, o 4-byte aligned).
+ *   kv_len : NULL, or a DEVICE pointer to B int32 values; keys j >= kv_len[b]
+ *            are masked for every query of batch b.  Values are clamped to
+ *            [0, N]; kv_len[b] = 0 gives O = 0 and lse = -inf for batch b.
+ */
+fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(int status);
+
+/* Detail of the last error returned on the calling thread (thread-local; ""
+ * when none). */
+const char* fa_last_error_string(void);
+
+/*
+ * fa_check_device_error -- synchronise `stream`, then read and clear the
+ * library's device status word on the current device.  Returns FA_ERR_TIMEOUT
+ * if any kernel since the last check gave up on a pipeline wait, FA_ERR_CUDA if
+ * the stream reported an error, else FA_OK.
+ */
+fa_status fa_check_device_error(void* stream);
+
+/*
+ * fa_set_wait_timeout_ms -- time limit for every pipeline wait inside the
+ * kernels (default 1000 ms; values < 1 are raised to 1).  Process-wide.
+ */
+void fa_set_wait_timeout_ms(int ms);
+
+/*
+ * fa_debug_inject -- test hook.  code 1 makes the next fa_fwd bf16 launches'
+ * producers stop feeding K/V tiles after the first one, so that the consumers'
+ * bounded waits run out and the launch reports FA_ERR_TIMEOUT.  code 0 (the
+ * default) turns it off.  Nothing faults, traps or hangs either way.
+ */
+void fa_debug_inject(int code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

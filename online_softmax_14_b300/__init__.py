@@ -8,15 +8,18 @@ input generator) imports without the library; every other name loads it on first
 use and raises if it has not been built.
 """
 
-_BINDING_NAMES = None
+import importlib
+
+_SUBMODULES = ("_binding", "inputs", "build")
 
 
 def __getattr__(name):
     if name.startswith("__"):
         raise AttributeError(name)
-    from . import _binding
-
+    if name in _SUBMODULES:
+        return importlib.import_module(f"{__name__}.{name}")
+    binding = importlib.import_module(f"{__name__}._binding")
     try:
-        return getattr(_binding, name)
+        return getattr(binding, name)
     except AttributeError:
-        raise AttributeError(f"module 'online_softmax_14_b300' has no attribute {name!r}") from None
+        raise AttributeError(f"module {__name__!r} has no attribute {name!r}") from None

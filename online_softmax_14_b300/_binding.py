@@ -1,0 +1,140 @@
+"""ctypes binding over libfa.so (include/fa.h).  Argument marshalling only.
+
+Each C entry point has a Python function of the same name taking the same
+arguments; a tensor argument may be a torch tensor (its ``data_ptr()`` is passed)
+or a raw integer address, and ``stream`` defaults to PyTorch's current CUDA
+stream.  A non-OK status raises ``FaError``.  ``attention_fwd`` is a convenience
+wrapper that allocates the outputs with PyTorch and calls ``fa_fwd_ex``.
+
+There is no fallback: if libfa.so has not been built, importing this module
+raises ImportError naming the build command.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build it with `python -m online_softmax_14_b300.build` "
+        "(or __graft_entry__.build()); there is no CPU fallback")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_BF16, FA_FP32 = 0, 1
+
+_vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_fwd.restype = _i
+_lib.fa_fwd_ex.argtypes = [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_fwd_ex.restype = _i
+_lib.fa_status_string.argtypes = [_i]
+_lib.fa_status_string.restype = ctypes.c_char_p
+_lib.fa_last_error_string.argtypes = []
+_lib.fa_last_error_string.restype = ctypes.c_char_p
+_lib.fa_check_device_error.argtypes = [_vp]
+_lib.fa_check_device_error.restype = _i
+_lib.fa_set_wait_timeout_ms.argtypes = [_i]
+_lib.fa_set_wait_timeout_ms.restype = None
+_lib.fa_debug_inject.argtypes = [_i]
+_lib.fa_debug_inject.restype = None
+_lib.fa_version.argtypes = []
+_lib.fa_version.restype = _i
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{fa_status_string(status)}: {detail}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int):
+    if status != FA_OK:
+        raise FaError(status, _lib.fa_last_error_string().decode())
+
+
+def fa_status_string(status: int) -> str:
+    return _lib.fa_status_string(int(status)).decode()
+
+
+def fa_last_error_string() -> str:
+    return _lib.fa_last_error_string().decode()
+
+
+def fa_version() -> int:
+    return _lib.fa_version()
+
+
+def fa_set_wait_timeout_ms(ms: int) -> None:
+    _lib.fa_set_wait_timeout_ms(int(ms))
+
+
+def fa_debug_inject(code: int) -> None:
+    _lib.fa_debug_inject(int(code))
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None) -> None:
+    _check(_lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
+                       _stream(stream)))
+
+
+def fa_fwd_ex(dtype, q, k, v, o, lse, kv_len, B, H, N, d, scale, causal, stream=None) -> None:
+    _check(_lib.fa_fwd_ex(int(dtype), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(kv_len), B, H, N, d,
+                          float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fa_check_device_error(stream=None) -> None:
+    _check(_lib.fa_check_device_error(_stream(stream)))
+
+
+def fa_status_raw(fn_name: str, *args) -> int:
+    """Call a C entry point by name with raw (already marshalled) arguments and
+    return its status code without raising (for tests of the error paths)."""
+    return getattr(_lib, fn_name)(*args)
+
+
+def attention_fwd(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
+    """O, lse = attention over [B, H, N, d] CUDA tensors (bf16 or fp32, contiguous).
+
+    Allocates O (same dtype as q) and lse (fp32) with PyTorch, then runs
+    ``fa_fwd_ex`` on ``stream`` (default: the current stream).
+    """
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype and t.shape == q.shape):
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype and shape [B, H, N, d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    fa_fwd_ex(FA_BF16 if q.dtype == torch.bfloat16 else FA_FP32, q, k, v, o, lse, kv_len, B, H, N, d, scale,
+              causal, stream)
+    return o, lse

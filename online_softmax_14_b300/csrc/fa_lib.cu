@@ -1,0 +1,269 @@
+// libfa: the C ABI declared in include/fa.h.  Host-side argument checks, TMA
+// tensor-map construction, kernel selection and launch, and the device status
+// word that the kernels' bounded waits report into.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "fa.h"
+#include "ptx.cuh"
+#include "fwd_simt.cuh"
+#include "fwd_tc.cuh"
+
+namespace fa {
+// Status word of the current device: kernels OR their timeout codes into it;
+// fa_check_device_error reads and clears it.
+__device__ unsigned int g_status_word;
+}  // namespace fa
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+constexpr int kStagesD128 = 3;
+constexpr int kStagesD64 = 4;
+
+thread_local char t_err[512] = "";
+std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};
+std::atomic<int> g_inject{0};
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  int cc_major = 0, cc_minor = 0;
+  unsigned int* status = nullptr;  // device address of fa::g_status_word
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Per-device set-up, done once with that device current: read the compute
+// capability, resolve the status word's device address, raise the kernels'
+// dynamic shared-memory limit.
+fa_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    if ((e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (s.cc_major != 10 || s.cc_minor != 3)
+      return fail(FA_ERR_UNSUPPORTED, "libfa is built for sm_103a; device %d is sm_%d%d", dev, s.cc_major,
+                  s.cc_minor);
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, fa::g_status_word)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    s.status = static_cast<unsigned int*>(addr);
+    using L128 = fa::TcLayout<128, kStagesD128>;
+    using L64 = fa::TcLayout<64, kStagesD64>;
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<128, kStagesD128>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L128::BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<64, kStagesD64>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L64::BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
+    s.ready = true;
+  }
+  *out = &s;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); 64 x 128 x 1 boxes with
+// 128-byte swizzle.  Rows past N read as zero.
+fa_status make_map(CUtensorMap* m, const void* base, int d, int N, int BH, const char* name) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+fa_status check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
+                       int N, int d, float scale, uintptr_t align) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID, "q, k, v and o must be non-null device pointers");
+  if (B < 1 || H < 1 || N < 1 || d < 1)
+    return fail(FA_ERR_INVALID, "sizes must be >= 1 (B=%d H=%d N=%d d=%d)", B, H, N, d);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID, "scale must be finite and > 0");
+  if (!aligned(q, align) || !aligned(k, align) || !aligned(v, align) || !aligned(o, align))
+    return fail(FA_ERR_INVALID, "q, k, v, o must be %d-byte aligned", (int)align);
+  if (lse && !aligned(lse, 4)) return fail(FA_ERR_INVALID, "lse must be 4-byte aligned");
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1ll << 30) || static_cast<long long>(N) * d > (1ll << 38))
+    return fail(FA_ERR_UNSUPPORTED, "problem too large (B*H=%lld, N*d=%lld)", bh, (long long)N * d);
+  return FA_OK;
+}
+
+template <int D, int STAGES>
+fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len, int B,
+                    int H, int N, float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
+  using L = fa::TcLayout<D, STAGES>;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  fa_status s;
+  if ((s = make_map(&mq, q, D, N, BH, "q")) != FA_OK) return s;
+  if ((s = make_map(&mk, k, D, N, BH, "k")) != FA_OK) return s;
+  if ((s = make_map(&mv, v, D, N, BH, "v")) != FA_OK) return s;
+  fa::TcParams p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.kv_len = kv_len;
+  p.BH = BH;
+  p.H = H;
+  p.N = N;
+  p.n_qt = (N + 127) / 128;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.status = ds.status;
+  p.timeout_ns = g_timeout_ns.load();
+  p.inject = g_inject.load();
+  const long long blocks = static_cast<long long>(p.n_qt) * BH;
+  if (blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  fa::fwd_bf16_tc_kernel<D, STAGES><<<static_cast<unsigned>(blocks), 256, L::BYTES, stream>>>(mq, mk, mv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc_kernel");
+  return FA_OK;
+}
+
+template <int DP>
+fa_status launch_simt(const fa::SimtParams& p, cudaStream_t stream) {
+  dim3 grid((p.N + fa::SIMT_ROWS - 1) / fa::SIMT_ROWS, p.BH);
+  fa::fwd_f32_simt_kernel<DP><<<grid, fa::SIMT_ROWS * 32, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch fwd_f32_simt_kernel");
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  t_err[0] = '\0';
+  fa_status s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_BF16) {
+    if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "bf16 path serves d = 64 or 128 (got %d)", d);
+    DeviceState* ds = nullptr;
+    if ((s = device_state(&ds)) != FA_OK) return s;
+    if (d == 128) return launch_tc<128, kStagesD128>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
+    return launch_tc<64, kStagesD64>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
+  }
+  if (dtype == FA_FP32) {
+    if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 4)) != FA_OK) return s;
+    if (d > 128) return fail(FA_ERR_UNSUPPORTED, "fp32 path serves d <= 128 (got %d)", d);
+    if (static_cast<long long>(B) * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fp32 path serves B*H <= 65535");
+    DeviceState* ds = nullptr;
+    if ((s = device_state(&ds)) != FA_OK) return s;
+    fa::SimtParams p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.o = static_cast<float*>(o);
+    p.lse = lse;
+    p.kv_len = kv_len;
+    p.BH = B * H;
+    p.H = H;
+    p.N = N;
+    p.d = d;
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.causal = causal ? 1 : 0;
+    if (d <= 32) return launch_simt<32>(p, st);
+    if (d <= 64) return launch_simt<64>(p, st);
+    if (d <= 96) return launch_simt<96>(p, st);
+    return launch_simt<128>(p, st);
+  }
+  return fail(FA_ERR_INVALID, "unknown dtype %d", dtype);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, void* stream) {
+  return fa_fwd_ex(FA_BF16, q, k, v, o, lse, nullptr, B, H, N, d, scale, causal, stream);
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID: return "FA_ERR_INVALID";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_UNKNOWN_STATUS";
+  }
+}
+
+const char* fa_last_error_string(void) { return t_err; }
+
+fa_status fa_check_device_error(void* stream) {
+  t_err[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  DeviceState* ds = nullptr;
+  fa_status s = device_state(&ds);
+  if (s != FA_OK) return s;
+  unsigned int word = 0, zero = 0;
+  if ((e = cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read status word");
+  if (word == 0) return FA_OK;
+  if ((e = cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "clear status word");
+  return fail(FA_ERR_TIMEOUT, "kernel pipeline wait timed out (status bits 0x%x)", word);
+}
+
+void fa_set_wait_timeout_ms(int ms) {
+  if (ms < 1) ms = 1;
+  g_timeout_ns.store(static_cast<unsigned long long>(ms) * 1000ull * 1000ull);
+}
+
+void fa_debug_inject(int code) { g_inject.store(code); }
+
+int fa_version(void) { return kVersion; }
+
+}  // extern "C"

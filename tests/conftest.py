@@ -11,3 +11,11 @@ if HERE not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
+
+
+def pytest_sessionstart(session):
+    # Build libfa.so in-tree if it is missing or older than its sources (nvcc
+    # cross-compiles without a GPU).
+    from online_softmax_14_b300.build import build_library
+
+    build_library()
