@@ -38,11 +38,12 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from online_softmax_14_b300.inputs import WORKLOADS, make_workload  # noqa: E402
+from online_softmax_14_b300.inputs import WORKLOADS, Workload, make_workload  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s at bf16 (causal halved) and % of B300 dense-BF16 peak"
 DEFAULT_WORKLOAD = "bf16_causal_B2_H32_N8192_d128"
 FALLBACK_BF16_TFLOPS = 1800.0  # used only when MEASURED_PEAKS.json is absent
+L2_BYTES = 126 * 1024 * 1024
 
 # DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture,
 # valid only for the kernel sources whose digest is recorded with it.
@@ -71,64 +72,104 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------------ clocks --
+REASON_BITS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons with NVML while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU in a
+    background thread, through NVML when importable, else an nvidia-smi
+    subprocess; only samples taken between mark_start() and mark_end() count."""
 
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
-
-    def __init__(self, device_index: int, period_s: float = 0.005):
-        self.samples, self.reasons, self.ok = [], set(), False
-        self.period = period_s
+    def __init__(self, device_index: int, period_ms: int = 20):
+        self.period_ms = period_ms
+        self.samples = []  # (monotonic time, sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.t0 = self.t1 = None
+        self.error = ""
+        props = torch.cuda.get_device_properties(device_index)
+        bus = getattr(props, "pci_bus_id", None)
+        self.pci = (f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+                    if bus is not None else None)
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.index = vis.split(",")[device_index] if vis else str(device_index)
+        self.nv = None
         try:
             import pynvml
 
             pynvml.nvmlInit()
-            props = torch.cuda.get_device_properties(device_index)
-            bus = getattr(props, "pci_bus_id", None)
-            if bus is not None:
-                pci = f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
-                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(pci)
-            else:
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.nv = pynvml
+            self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(self.pci) if self.pci
+                      else pynvml.nvmlDeviceGetHandleByIndex(int(self.index)))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # NVML unavailable: report that instead of clocks
-            self.err = repr(e)
+            self.nv = pynvml
+        except Exception as e:
+            self.error = f"nvml: {e!r}"
 
-    def _run(self):
+    def _nvml_loop(self):
         nv = self.nv
-        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             nv.nvmlDeviceGetCurrentClocksThrottleReasons
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                r = get_reasons(self.h)
-                for bit, name in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(name)
+                self.samples.append((time.monotonic(), nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM),
+                                     int(get_r(self.h))))
             except Exception:
                 pass
-            time.sleep(self.period)
+            time.sleep(self.period_ms / 1000)
+
+    def _smi_loop(self):
+        import subprocess
+
+        cmd = ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", str(self.period_ms), "-i", self.pci or self.index]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:
+            self.error += f"; nvidia-smi: {e!r}"
+            return
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                self.max_mhz = float(parts[1])
+                self.samples.append((time.monotonic(), float(parts[0]), int(parts[2], 16)))
+            except (ValueError, IndexError):
+                continue
 
     def __enter__(self):
-        if self.ok:
-            self._stop = threading.Event()
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        self._stop = threading.Event()
+        self._proc = None
+        self._t = threading.Thread(target=self._nvml_loop if self.nv else self._smi_loop, daemon=True)
+        self._t.start()
+        deadline = time.monotonic() + 3.0  # let the first sample arrive
+        while not self.samples and time.monotonic() < deadline:
+            time.sleep(0.01)
         return self
 
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
+
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self._t.join()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+        self._t.join(timeout=5)
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "err", "")}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        inside = [s for s in self.samples if self.t0 is not None and self.t0 <= s[0] <= (self.t1 or 1e30)]
+        reasons = set()
+        for _, _, r in inside:
+            for bit, name in REASON_BITS.items():
+                if r & bit:
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median([s[1] for s in inside]) if inside else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons), "samples": len(inside),
+               "source": "nvml" if self.nv else "nvidia-smi"}
+        if not inside and self.error:
+            out["error"] = self.error
+        return out
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -173,12 +214,15 @@ def cpu_baseline(w, inputs, budget_s=15.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d: a custom bf16 workload instead of --workload (profiling runs)")
+    ap.add_argument("--causal", type=int, default=1, help="with --shape: causal mask (1) or not (0)")
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--e2e-steps", type=int, default=10, help="0 skips the end-to-end measurement")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="0 skips the CPU oracle baseline")
     ap.add_argument("--seed", type=int, default=0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -187,7 +231,12 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    w = WORKLOADS[args.workload]
+    if args.shape:
+        B, H, N, d = (int(x) for x in args.shape.split(","))
+        w = Workload(f"bf16_{'causal' if args.causal else 'full'}_B{B}_H{H}_N{N}_d{d}", "bf16", B, H, N, d,
+                     bool(args.causal))
+    else:
+        w = WORKLOADS[args.workload]
 
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
@@ -216,17 +265,18 @@ def main():
         step()
     fa.fa_check_device_error(stream)
 
-    clk = ClockSampler(local)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with clk:
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     if dist:
         dist.barrier()
     fa.fa_check_device_error(stream)
@@ -237,15 +287,64 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_max = float(t.item())
     f_step = flops_per_step(w)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
     value = f_step * world / (ms_max * 1e-3) / 1e12
     achieved = f_step / (ms * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs -> device -> kernel -> host outputs
+    e2e = run_e2e(args, w, inputs, step, q, k, v, kv, o, lse, stream, dev, dist, world, fa) \
+        if args.e2e_steps > 0 else None
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    digest = kernel_src_digest()
+    tr = NCU_TRAFFIC.get(w.name)
+    traffic = tr["bytes"] if tr and tr["src_digest"] == digest else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1), see online_softmax_14_b300/inputs.py)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "seed": args.seed, "inputs_exceed_l2": in_bytes > L2_BYTES, "l2_flush": False,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "src_digest": digest},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    if rank == 0 and world == 1 and args.cpu_budget_s > 0:
+        line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, inputs, step, q, k, v, kv, o, lse, stream, dev, dist, world, fa):
+    """Same metric through the public API with host buffers: every step copies
+    Q, K, V (and kv_len) from pinned host memory, runs the kernel, and copies O
+    and lse back to pinned host memory, all inside the timed region."""
+    f_step = flops_per_step(w)
     hq, hk, hv = (inputs[n].pin_memory() for n in ("q", "k", "v"))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    hkv = None
     if kv is not None:
         hkv = inputs["kv_len"].pin_memory()
         h2d += hkv.numel() * hkv.element_size()
@@ -254,7 +353,7 @@ def main():
         q.copy_(hq, non_blocking=True)
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
-        if kv is not None:
+        if hkv is not None:
             kv.copy_(hkv, non_blocking=True)
         step()
         ho.copy_(o, non_blocking=True)
@@ -277,45 +376,8 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_e2e = float(t.item())
     e2e_value = f_step * world / (ms_e2e * 1e-3) / 1e12
-
-    peaks, peak_src = measured_peaks()
-    peak = float(peaks["bf16_tflops"])
-    digest = kernel_src_digest()
-    tr = NCU_TRAFFIC.get(w.name)
-    traffic = tr["bytes"] if tr and tr["src_digest"] == digest else None
-
-    line = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_max, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": w.dtype,
-        "data": "synthetic (seeded N(0,1), see online_softmax_14_b300/inputs.py)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-                   "seed": args.seed, "inputs_exceed_l2": True, "l2_flush": False,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops (burst)", "src_digest": digest},
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)},
-        "gpu_launches": args.steps,
-        "clocks": clk.summary(),
-        "gpu": torch.cuda.get_device_name(dev),
-    }
-    if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_budget_s)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.barrier()
-        dist.destroy_process_group()
+    return {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)}
 
 
 def run_reference(args, w, rank, world):

@@ -103,9 +103,10 @@ __global__ void __launch_bounds__(256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest causal tiles first: block x -> (query tile counted from the end, head)
-  const int qt = p.n_qt - 1 - static_cast<int>(blockIdx.x) / p.BH;
-  const int bh = static_cast<int>(blockIdx.x) % p.BH;
+  // Head-major order: consecutive CTAs share one head's K/V, which then stays in
+  // L2; within a head the heaviest causal tiles go first.
+  const int bh = static_cast<int>(blockIdx.x) / p.n_qt;
+  const int qt = p.n_qt - 1 - static_cast<int>(blockIdx.x) % p.n_qt;
   const int b = bh / p.H;
   const int q0 = qt * L::BM;
   int kv_limit = p.N;
@@ -256,23 +257,30 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) sr[i] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // row max as a tree: 8 independent chains, then combine
+      float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+      for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(sr[t]);
+#pragma unroll
+      for (int i = 8; i < 128; i += 8)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(mx8[t], __uint_as_float(sr[i + t]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_blk = mx * sl;
       const float m_new = (m_blk > m + 8.f) ? m_blk : m;  // lazy reference move
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float c = ex2_approx(m - m_ref);               // 0 on the first block, 1 if unchanged
-      float rs = 0.f;
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in 4 independent chains
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl, -m_ref));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl, -m_ref));
-        rs += p0 + p1;
+        rs4[i & 3] += p0 + p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
-      l = l * c + rs;
+      l = l * c + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
       const uint32_t p_col = lane_base + (sb ? L::TM_P1 : L::TM_P0);
       FA_TMEM_ST32(p_col + 0, pk + 0);
       FA_TMEM_ST32(p_col + 32, pk + 32);
