@@ -14,7 +14,10 @@ carries:
   * e2e       -- the same metric through the public API with the inputs copied
                  from pinned host memory and O, lse copied back inside each step;
   * cpu_baseline -- the float64 CPU oracle timed on a bounded sample (rank 0, N=1);
-  * clocks    -- SM clocks and throttle reasons sampled during the timed region.
+  * clocks    -- SM clocks and throttle reasons sampled during the timed region;
+  * fwd_bwd   -- forward and backward (recompute) TFLOP/s of the training
+                 workload, bf16 causal B=4 H=16 N=4096 d=128 (backward FLOPs
+                 10*B*H*N^2*d, halved for causal).
 With --impl reference the float64 oracle itself is timed (rank 0 only).
 Multi-GPU (torchrun): every rank runs its own replica of the workload, no data
 exchange; value = all ranks' FLOPs / the slowest rank's time ("weak" scaling).
@@ -42,6 +45,7 @@ from online_softmax_14_b300.inputs import WORKLOADS, Workload, make_workload  # 
 
 METRIC = "attention fwd TFLOP/s at bf16 (causal halved) and % of B300 dense-BF16 peak"
 DEFAULT_WORKLOAD = "bf16_causal_B2_H32_N8192_d128"
+BWD_WORKLOAD = "bf16_causal_fwdbwd_B4_H16_N4096_d128"
 FALLBACK_BF16_TFLOPS = 1800.0  # used only when MEASURED_PEAKS.json is absent
 L2_BYTES = 126 * 1024 * 1024
 
@@ -52,6 +56,12 @@ NCU_TRAFFIC = {}  # {workload: {"bytes": int, "src_digest": str}}
 
 def flops_per_step(w) -> float:
     f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    return f / 2 if w.causal else f
+
+
+def bwd_flops(w) -> float:
+    """Five N x N x d products per head (S, dP, dV, dK, dQ), halved for causal."""
+    f = 10.0 * w.B * w.H * w.N * w.N * w.d
     return f / 2 if w.causal else f
 
 
@@ -224,6 +234,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10, help="0 skips the end-to-end measurement")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="0 skips the CPU oracle baseline")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--bwd-steps", type=int, default=20,
+                    help="timed steps of the forward + backward workload (0 skips it)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -325,6 +337,8 @@ def main():
         "clocks": clk.summary(),
         "gpu": torch.cuda.get_device_name(dev),
     }
+    if args.bwd_steps > 0 and not args.shape:
+        line["fwd_bwd"] = run_fwd_bwd(args, fa, dev, stream, dist)
     if rank == 0 and world == 1 and args.cpu_budget_s > 0:
         line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_budget_s)
     if rank == 0:
@@ -332,6 +346,52 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_fwd_bwd(args, fa, dev, stream, dist):
+    """Forward and backward of the training workload (bf16, causal, B=4 H=16
+    N=4096 d=128, dO drawn after Q, K, V), each timed over --bwd-steps launches
+    with CUDA events on the launching stream.  The backward is one fa_bwd call
+    (two kernels: the row preprocess and the main tensor-core kernel)."""
+    w = WORKLOADS[BWD_WORKLOAD]
+    inp = make_workload(w, seed=args.seed)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        fa.fa_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, inp["scale"], w.causal, stream)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, w.B, w.H, w.N, w.d, inp["scale"], w.causal, stream)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.bwd_steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.bwd_steps
+
+    ms_f = timed(fwd)
+    ms_b = timed(bwd)
+    fa.fa_check_device_error(stream)
+    ff, fb = flops_per_step(w), bwd_flops(w)
+    return {"workload": w.name, "steps": args.bwd_steps, "fwd_ms": round(ms_f, 4), "bwd_ms": round(ms_b, 4),
+            "fwd_tflops": round(ff / ms_f / 1e9, 2), "bwd_tflops": round(fb / ms_b / 1e9, 2),
+            "fwd_bwd_tflops": round((ff + fb) / (ms_f + ms_b) / 1e9, 2),
+            "flops": {"fwd": ff, "bwd": fb, "bwd_formula": "10*B*H*N^2*d, halved for causal"},
+            "gpu_launches_per_bwd": 2}
 
 
 def run_e2e(args, w, inputs, step, q, k, v, kv, o, lse, stream, dev, dist, world, fa):

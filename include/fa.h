@@ -75,6 +75,46 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
                     const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/*
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd / fa_bwd_ex need for
+ * this problem: two float32 arrays of B*H*Np entries, Np = N rounded up to a
+ * multiple of 64 (per-row D = rowsum(dO * O) and lse * log2(e)).  Returns 0 for
+ * non-positive sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_bwd -- attention backward by recomputation, bfloat16 inputs, float32
+ * gradients.  The probabilities are rebuilt from q, k and the forward's lse
+ * instead of being read from a stored N x N matrix ("Question bank -- Flash
+ * attention and efficient attention", the recomputation items); the gradient is
+ * that of L = sum(O * dO) for the forward above:
+ *     dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P * (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, k, v, o, dO : const bf16*, [B, H, N, d], 16-byte aligned; o and lse are
+ *                    the outputs of fa_fwd for the same q, k, v, scale, causal.
+ *   lse            : const float*, [B, H, N] (required).
+ *   dq, dk, dv     : float*, [B, H, N, d], 16-byte aligned; written (dq is
+ *                    zeroed by the call, then accumulated).
+ *   workspace      : device memory of at least fa_bwd_workspace_size(B, H, N, d)
+ *                    bytes, 16-byte aligned, owned by the caller; its contents
+ *                    on entry do not matter and are overwritten.
+ *   d              : 128 (else FA_ERR_UNSUPPORTED).
+ * Asynchronous on `stream` like every call here; the library allocates nothing.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, void* stream);
+
+/*
+ * fa_bwd_ex -- as fa_bwd, with the key-padding lengths of fa_fwd_ex: kv_len is
+ * NULL or a DEVICE pointer to B int32 values (clamped to [0, N]); keys
+ * j >= kv_len[b] get zero probability, so their dK and dV rows are zero.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                    int B, int H, int N, int d, float scale, int causal, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* fa_status_string(int status);
 

@@ -44,6 +44,13 @@ _lib.fa_debug_inject.argtypes = [_i]
 _lib.fa_debug_inject.restype = None
 _lib.fa_version.argtypes = []
 _lib.fa_version.restype = _i
+_sz = ctypes.c_size_t
+_lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
+_lib.fa_bwd_workspace_size.restype = _sz
+_lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_bwd.restype = _i
+_lib.fa_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_bwd_ex.restype = _i
 
 
 class FaError(RuntimeError):
@@ -107,6 +114,24 @@ def fa_fwd_ex(dtype, q, k, v, o, lse, kv_len, B, H, N, d, scale, causal, stream=
                           float(scale), int(bool(causal)), _stream(stream)))
 
 
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(_lib.fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+           stream=None) -> None:
+    _check(_lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                       _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale), int(bool(causal)),
+                       _stream(stream)))
+
+
+def fa_bwd_ex(q, k, v, o, do, lse, kv_len, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+              stream=None) -> None:
+    _check(_lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(kv_len), _ptr(dq),
+                          _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale),
+                          int(bool(causal)), _stream(stream)))
+
+
 def fa_check_device_error(stream=None) -> None:
     _check(_lib.fa_check_device_error(_stream(stream)))
 
@@ -138,3 +163,26 @@ def attention_fwd(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
     fa_fwd_ex(FA_BF16 if q.dtype == torch.bfloat16 else FA_FP32, q, k, v, o, lse, kv_len, B, H, N, d, scale,
               causal, stream)
     return o, lse
+
+
+def attention_bwd(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, stream=None):
+    """dQ, dK, dV (float32) of attention over bf16 [B, H, N, d] CUDA tensors.
+
+    ``o`` and ``lse`` are the forward's outputs for the same inputs.  Allocates
+    the gradients and the workspace with PyTorch, then runs ``fa_bwd_ex``.
+    """
+    for t in (q, k, v, o, do):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16 and t.shape == q.shape):
+            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors of shape [B, H, N, d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    ws_bytes = fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    fa_bwd_ex(q, k, v, o, do, lse.contiguous(), kv_len, dq, dk, dv, ws, ws_bytes, B, H, N, d, scale, causal, stream)
+    return dq, dk, dv

@@ -17,6 +17,7 @@
 #include "ptx.cuh"
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
+#include "bwd_tc.cuh"
 
 namespace fa {
 // Status word of the current device: kernels OR their timeout codes into it;
@@ -26,10 +27,11 @@ __device__ unsigned int g_status_word;
 
 namespace {
 
-constexpr int kVersion = 100;  // 0.1.0
+constexpr int kVersion = 200;  // 0.2.0
 constexpr int kMaxDevices = 64;
 constexpr int kStagesD128 = 3;
 constexpr int kStagesD64 = 4;
+constexpr int kStagesBwd = 2;
 
 thread_local char t_err[512] = "";
 std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};
@@ -85,6 +87,9 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<64, kStagesD64>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L64::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
+    if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  fa::BwdLayout<kStagesBwd>::BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
     s.ready = true;
   }
   *out = &s;
@@ -105,14 +110,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); 64 x 128 x 1 boxes with
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); 64 x rows x 1 boxes with
 // 128-byte swizzle.  Rows past N read as zero.
-fa_status make_map(CUtensorMap* m, const void* base, int d, int N, int BH, const char* name) {
+fa_status make_map(CUtensorMap* m, const void* base, int d, int N, int BH, const char* name, int rows = 128) {
   auto enc = encode_fn();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -178,6 +183,68 @@ fa_status launch_simt(const fa::SimtParams& p, cudaStream_t stream) {
   return FA_OK;
 }
 
+// Row stride of the backward workspace arrays: N rounded up to the 64-query tile.
+long long bwd_np(int N) { return (static_cast<long long>(N) + 63) / 64 * 64; }
+
+size_t bwd_ws_bytes(int B, int H, int N) {
+  return static_cast<size_t>(2) * static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(bwd_np(N)) *
+         sizeof(float);
+}
+
+fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                     const int32_t* kv_len, float* dq, float* dk, float* dv, float* ws, int B, int H, int N,
+                     float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
+  constexpr int D = 128;
+  using L = fa::BwdLayout<kStagesBwd>;
+  const int BH = B * H;
+  const long long Np = bwd_np(N);
+  const long long pre_blocks = static_cast<long long>(BH) * (Np / 64);
+  const long long n_kt = (N + L::BN - 1) / L::BN;
+  const long long blocks = n_kt * BH;
+  if (pre_blocks > 0x7fffffffll || blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+
+  fa::BwdPreParams pp{};
+  pp.o = static_cast<const __nv_bfloat16*>(o);
+  pp.dO = static_cast<const __nv_bfloat16*>(dO);
+  pp.lse = lse;
+  pp.dq = dq;
+  pp.lse2 = ws;
+  pp.dd = ws + static_cast<size_t>(BH) * Np;
+  pp.BH = BH;
+  pp.N = N;
+  pp.Np = static_cast<int>(Np);
+  fa::bwd_preprocess_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(pp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch bwd_preprocess_kernel");
+
+  CUtensorMap mq, mk, mv, mdo;
+  fa_status s;
+  if ((s = make_map(&mq, q, D, N, BH, "q", 64)) != FA_OK) return s;
+  if ((s = make_map(&mk, k, D, N, BH, "k", 128)) != FA_OK) return s;
+  if ((s = make_map(&mv, v, D, N, BH, "v", 128)) != FA_OK) return s;
+  if ((s = make_map(&mdo, dO, D, N, BH, "dO", 64)) != FA_OK) return s;
+  fa::BwdParams p{};
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.lse2 = pp.lse2;
+  p.dd = pp.dd;
+  p.kv_len = kv_len;
+  p.BH = BH;
+  p.H = H;
+  p.N = N;
+  p.Np = static_cast<int>(Np);
+  p.n_kt = static_cast<int>(n_kt);
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.status = ds.status;
+  p.timeout_ns = g_timeout_ns.load();
+  fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_bf16_tc_kernel");
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -226,6 +293,39 @@ fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, void* stream) {
   return fa_fwd_ex(FA_BF16, q, k, v, o, lse, nullptr, B, H, N, d, scale, causal, stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  return bwd_ws_bytes(B, H, N);
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                    int B, int H, int N, int d, float scale, int causal, void* stream) {
+  t_err[0] = '\0';
+  fa_status s;
+  if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
+  if (!dO || !lse || !dq || !dk || !dv || !workspace)
+    return fail(FA_ERR_INVALID, "dO, lse, dq, dk, dv and workspace must be non-null device pointers");
+  if (!aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 16))
+    return fail(FA_ERR_INVALID, "dO, dq, dk, dv and workspace must be 16-byte aligned");
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "bf16 backward serves d = 128 (got %d)", d);
+  const size_t need = bwd_ws_bytes(B, H, N);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes,
+                need);
+  DeviceState* ds = nullptr;
+  if ((s = device_state(&ds)) != FA_OK) return s;
+  return launch_bwd(q, k, v, o, dO, lse, kv_len, dq, dk, dv, static_cast<float*>(workspace), B, H, N, scale, causal,
+                    static_cast<cudaStream_t>(stream), *ds);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, void* stream) {
+  return fa_bwd_ex(q, k, v, o, dO, lse, nullptr, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                   stream);
 }
 
 const char* fa_status_string(int status) {

@@ -91,3 +91,33 @@ def test_valid_call_without_gpu_fails_loudly():
     assert fa.fa_last_error_string()
     with pytest.raises(B.FaError):
         fa.fa_fwd(P, P, P, P, None, 1, 1, 16, 64, 0.125, False, stream=0)
+
+
+def _bwd(q=P, k=P, v=P, o=P, do=P, lse=P, kv=None, dq=P, dk=P, dv=P, ws=P, ws_bytes=1 << 20, Bs=1, H=1, N=16, d=128,
+         scale=0.125, causal=0):
+    return B.fa_status_raw("fa_bwd_ex", q, k, v, o, do, lse, kv, dq, dk, dv, ws, ctypes.c_size_t(ws_bytes), Bs, H, N,
+                           d, ctypes.c_float(scale), causal, None)
+
+
+def test_bwd_workspace_size():
+    # two float32 arrays of B*H*Np, Np = N rounded up to 64
+    assert fa.fa_bwd_workspace_size(2, 3, 100, 128) == 2 * 2 * 3 * 128 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 64, 128) == 2 * 64 * 4
+    assert fa.fa_bwd_workspace_size(0, 1, 64, 128) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(do=None), B.FA_ERR_INVALID),
+    (dict(lse=None), B.FA_ERR_INVALID),
+    (dict(dq=None), B.FA_ERR_INVALID),
+    (dict(ws=None), B.FA_ERR_INVALID),
+    (dict(dk=P + 4), B.FA_ERR_INVALID),
+    (dict(ws=P + 8), B.FA_ERR_INVALID),
+    (dict(ws_bytes=16), B.FA_ERR_INVALID),      # smaller than fa_bwd_workspace_size
+    (dict(N=0), B.FA_ERR_INVALID),
+    (dict(scale=float("nan")), B.FA_ERR_INVALID),
+    (dict(d=64), B.FA_ERR_UNSUPPORTED),
+])
+def test_bwd_host_validation(kw, status):
+    assert _bwd(**kw) == status
+    assert fa.fa_last_error_string() != ""

@@ -1,0 +1,133 @@
+"""GPU parity of the backward kernels against the float64 oracle (needs a B300).
+
+The CUDA path runs the forward (for O and lse) and then the backward on the same
+bf16 inputs; the oracle differentiates the exact attention definition from the
+same bf16-rounded Q, K, V, dO converted to float64.  Tolerance per gradient
+tensor (dQ, dK, dV, all float32): max |g - g_ref| <= 2e-2 and
+mean |g - g_ref| <= 2e-3, the bf16 forward's bar.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_14_b300.inputs import WORKLOADS, make_problem, make_workload
+
+pytestmark = pytest.mark.gpu
+
+G_MAX, G_MEAN = 2e-2, 2e-3
+DEV = "cuda:0"
+
+
+def fa():
+    import online_softmax_14_b300 as m
+    return m
+
+
+def run_fwd_bwd(pr, causal, kv_len=None):
+    q, k, v, do = (pr[n].to(DEV) for n in ("q", "k", "v", "do"))
+    kl = kv_len if kv_len is not None else pr.get("kv_len")
+    o, lse = fa().attention_fwd(q, k, v, pr["scale"], causal=causal, kv_len=kl)
+    dq, dk, dv = fa().attention_bwd(q, k, v, o, lse, do, pr["scale"], causal=causal, kv_len=kl)
+    fa().fa_check_device_error()
+    return tuple(t.cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+
+
+# Large-logit inputs (Q, K x 8) give gradients of magnitude ~25; there the bar
+# is relative to the largest oracle gradient.  The kernel rounds P and dS to
+# bf16 (relative error <= 2^-9 each) before the tensor-core products, so a few
+# bf16 ulps of the gradient's scale, 1e-2, is the bound.
+G_REL = 1e-2
+
+
+def check_grads(got, ref, label, relative=False):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.all(np.isfinite(g)), f"{label} {name}: non-finite"
+        err = np.abs(g - r)
+        if relative:
+            scale = max(1.0, float(np.abs(r).max()))
+            assert err.max() <= G_REL * scale, f"{label} {name}: max err {err.max():.3g} vs scale {scale:.3g}"
+            continue
+        assert err.max() <= G_MAX, f"{label} {name}: max err {err.max():.3g} (|ref| max {np.abs(r).max():.3g})"
+        assert err.mean() <= G_MEAN, f"{label} {name}: mean err {err.mean():.3g}"
+
+
+def bwd_parity(B, H, N, causal, seed=0, kv_len=None, padded=False, qk_mul=1.0, relative=False):
+    pr = make_problem(B, H, N, 128, "bf16", seed=seed, backward=True, padded=padded, kv_len=kv_len,
+                      qk_mul=qk_mul)
+    got = run_fwd_bwd(pr, causal)
+    kl = None if pr["kv_len"] is None else pr["kv_len"].tolist()
+    ref = oracle.attention_bwd(pr["q"], pr["k"], pr["v"], pr["do"], pr["scale"], causal=causal, kv_len=kl)
+    check_grads(got, ref, f"B{B} H{H} N{N} c{causal} kv{kl}", relative=relative)
+    return got, ref
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [64, 128, 200, 384])
+def test_bwd_small(N, causal):
+    # N = 200: two 128-key tiles, the last one ragged; four 64-query tiles, the last ragged
+    bwd_parity(2, 2, N, causal, seed=N + causal)
+
+
+@pytest.mark.parametrize("N", [1, 17, 63, 65, 129, 255, 257])
+def test_bwd_sequence_lengths(N):
+    bwd_parity(1, 2, N, causal=(N % 2 == 1), seed=N)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_key_padding(causal):
+    N = 300
+    kv = [0, 1, 64, 127, 128, 129, 299, 300]
+    (dq, dk, dv), _ = bwd_parity(len(kv), 2, N, causal, seed=11, kv_len=kv)
+    # batch 0 sees no key: its probabilities are all zero, so every gradient is zero
+    assert np.all(dq[0] == 0) and np.all(dk[0] == 0) and np.all(dv[0] == 0)
+    # keys at or past kv_len have no probability mass, hence zero dK and dV rows
+    for b, n in enumerate(kv):
+        assert np.all(dk[b, :, n:] == 0) and np.all(dv[b, :, n:] == 0)
+
+
+def test_bwd_large_logits():
+    """Q and K scaled by 8 (logits of several hundred): P is nearly one-hot and
+    the gradients stay finite and accurate relative to their magnitude."""
+    bwd_parity(2, 2, 256, causal=False, seed=12, padded=True, qk_mul=8.0, relative=True)
+
+
+def test_bwd_dv_closed_form_uniform():
+    """Q = 0 makes every score equal (Worked examples, Cell C), so P is uniform over
+    the visible keys: with the causal mask dV_j = sum_{i >= j} dO_i / (i + 1), and
+    dK = scale dS^T Q is exactly zero."""
+    B, H, N = 1, 2, 192
+    pr = make_problem(B, H, N, 128, "bf16", seed=13, backward=True)
+    pr["q"] = torch.zeros_like(pr["q"])
+    dq, dk, dv = run_fwd_bwd(pr, causal=True)
+    do = pr["do"].double().numpy()
+    w = do / np.arange(1, N + 1)[None, None, :, None]           # dO_i / (i + 1)
+    want = np.cumsum(w[:, :, ::-1], axis=2)[:, :, ::-1]          # sum over i >= j
+    assert np.abs(dv - want).max() <= G_MAX and np.abs(dv - want).mean() <= G_MEAN
+    assert np.all(dk == 0)
+
+
+def test_bwd_full_size_workload_sampled_heads():
+    """The forward + backward workload (B=4 H=16 N=4096 d=128, causal) in the exact
+    launch configuration the benchmark uses; two whole heads are compared with
+    the oracle, every gradient is checked finite."""
+    w = WORKLOADS["bf16_causal_fwdbwd_B4_H16_N4096_d128"]
+    pr = make_workload(w)
+    dq, dk, dv = run_fwd_bwd(pr, w.causal)
+    for t in (dq, dk, dv):
+        assert np.all(np.isfinite(t))
+    for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.attention_bwd(pr["q"][sl], pr["k"][sl], pr["v"][sl], pr["do"][sl], pr["scale"], causal=True)
+        check_grads((dq[sl], dk[sl], dv[sl]), ref, f"{w.name} head ({b},{h})")
+
+
+def test_bwd_repeatable():
+    """Two calls on the same inputs agree (dQ is accumulated with atomics, so only
+    the summation order may differ)."""
+    pr = make_problem(1, 2, 256, 128, "bf16", seed=14, backward=True)
+    a = run_fwd_bwd(pr, causal=True)
+    b = run_fwd_bwd(pr, causal=True)
+    for x, y in zip(a, b):
+        assert np.abs(x - y).max() <= 1e-5
