@@ -115,6 +115,34 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
                     int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
+ * The source pages have no counterpart: it exists only because of how some
+ * callers manage memory.  A caller that cannot call cudaMalloc when it needs a
+ * gradient cannot hand fa_bwd a workspace.  That includes code running inside
+ * an allocator's own hooks, runtimes whose device pool is fixed and fully
+ * handed out at start-up, and hosts whose policy forbids allocation after
+ * initialisation.  This call instead uses a fixed device array inside the
+ * library (2 * FA_BWD_NOALLOC_MAX_ROWS floats, 4 MiB).  Every GPU that loads
+ * the library holds that array until the process exits.
+ *   Arguments are those of fa_bwd without the workspace; q, k, v, o, dO, lse,
+ *   dq, dk, dv are still the caller's device memory.  The library allocates
+ *   nothing, through the CUDA runtime or otherwise.
+ *   Limit: B * H * Np <= FA_BWD_NOALLOC_MAX_ROWS, where Np is N rounded up to
+ *   a multiple of 64.  Larger problems return FA_ERR_UNSUPPORTED with a message
+ *   naming the limit; use fa_bwd with a workspace for them.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress, so make that first call before any stream capture.
+ *   All calls share the one array.  Calls whose work overlaps on the GPU (say,
+ *   on two streams without ordering) corrupt each other's gradients; order
+ *   them.  Stale contents left by an earlier call are harmless: every part of
+ *   the array a call reads is first written by that call.
+ */
+#define FA_BWD_NOALLOC_MAX_ROWS 524288
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, float* dq, float* dk, float* dv, int B, int H, int N, int d, float scale,
+                         int causal, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* fa_status_string(int status);
 

@@ -51,6 +51,9 @@ _lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _
 _lib.fa_bwd.restype = _i
 _lib.fa_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_bwd_ex.restype = _i
+_lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_bwd_noalloc.restype = _i
+FA_BWD_NOALLOC_MAX_ROWS = 524288
 
 
 class FaError(RuntimeError):
@@ -130,6 +133,13 @@ def fa_bwd_ex(q, k, v, o, do, lse, kv_len, dq, dk, dv, workspace, workspace_byte
     _check(_lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(kv_len), _ptr(dq),
                           _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale),
                           int(bool(causal)), _stream(stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, stream=None) -> None:
+    """fa_bwd without a workspace argument: the library uses its own fixed
+    device scratch (for callers that cannot allocate device memory)."""
+    _check(_lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _stream(stream)))
 
 
 def fa_check_device_error(stream=None) -> None:

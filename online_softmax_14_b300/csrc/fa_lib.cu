@@ -367,3 +367,74 @@ void fa_debug_inject(int code) { g_inject.store(code); }
 int fa_version(void) { return kVersion; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------
+// Backward without any allocation.
+//
+// Some callers cannot allocate device memory at the moment they need a
+// gradient. Examples: code that runs inside a custom allocator's own callbacks,
+// a runtime whose memory pool is fixed and fully handed out at start-up, and
+// embedded hosts whose policy forbids cudaMalloc after initialisation. They
+// cannot provide the backward's workspace, so for them the library keeps it in
+// a fixed device array that is part of the loaded module. Every GPU that loads
+// the library holds this array until the process exits.
+//
+// Limit: the workspace is two float32 arrays of B*H*Np rows (Np = N rounded up
+// to 64), so B*H*Np may be at most FA_BWD_NOALLOC_MAX_ROWS (4 MiB in total).
+// Calls share the array: two calls that run at the same time on the GPU (for
+// instance on different streams) overwrite each other's workspace and give
+// wrong gradients, so such calls must be ordered. Nothing in the array needs to
+// start at zero. Every row a call reads has first been written by that same
+// call's preprocess kernel, so stale contents from an earlier call do no harm.
+namespace {
+
+static __device__ __align__(256) float g_bwd_noalloc_scratch[2 * FA_BWD_NOALLOC_MAX_ROWS];
+
+float* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// The array's device address for the current device, looked up once per device
+// with that device current (the host-side name of the array is only a stand-in
+// and must never be handed to a kernel).
+fa_status noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, g_bwd_noalloc_scratch)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(backward scratch)");
+    g_noalloc_ptr[dev] = static_cast<float*>(addr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                    const float* lse, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+                                    float scale, int causal, void* stream) {
+  t_err[0] = '\0';
+  fa_status s;
+  if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
+  if (!dO || !lse || !dq || !dk || !dv)
+    return fail(FA_ERR_INVALID, "dO, lse, dq, dk and dv must be non-null device pointers");
+  if (!aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return fail(FA_ERR_INVALID, "dO, dq, dk and dv must be 16-byte aligned");
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "bf16 backward serves d = 128 (got %d)", d);
+  const long long rows = static_cast<long long>(B) * H * bwd_np(N);
+  if (rows > FA_BWD_NOALLOC_MAX_ROWS)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_bwd_noalloc: B*H*Np = %lld rows (Np = N rounded up to 64) exceeds its fixed scratch of %d rows; "
+                "use fa_bwd with a caller-supplied workspace",
+                rows, (int)FA_BWD_NOALLOC_MAX_ROWS);
+  DeviceState* ds = nullptr;
+  if ((s = device_state(&ds)) != FA_OK) return s;
+  float* ws = nullptr;
+  if ((s = noalloc_scratch(&ws)) != FA_OK) return s;
+  return launch_bwd(q, k, v, o, dO, lse, nullptr, dq, dk, dv, ws, B, H, N, scale, causal,
+                    static_cast<cudaStream_t>(stream), *ds);
+}
