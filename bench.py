@@ -236,6 +236,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--bwd-steps", type=int, default=20,
                     help="timed steps of the forward + backward workload (0 skips it)")
+    ap.add_argument("--bwd-shape", default=None,
+                    help="B,H,N: a custom causal d=128 forward + backward workload (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -354,6 +356,9 @@ def run_fwd_bwd(args, fa, dev, stream, dist):
     with CUDA events on the launching stream.  The backward is one fa_bwd call
     (two kernels: the row preprocess and the main tensor-core kernel)."""
     w = WORKLOADS[BWD_WORKLOAD]
+    if args.bwd_shape:
+        B, H, N = (int(x) for x in args.bwd_shape.split(","))
+        w = Workload(f"bf16_causal_fwdbwd_B{B}_H{H}_N{N}_d128", "bf16", B, H, N, 128, True, backward=True)
     inp = make_workload(w, seed=args.seed)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)

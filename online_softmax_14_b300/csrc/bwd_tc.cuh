@@ -22,6 +22,8 @@
 //       MMA3  dV    += P^T_t dO_t          (128 x d, TMEM; A = P^T from TMEM)
 //       MMA4  dK    += dS^T_t Q_t          (128 x d, TMEM; A = dS^T from SMEM)
 //       MMA5  dQ^T_t = K^T dS_t            (d x 64, TMEM; A = K read MN-major)
+//    issued in the order MMA3_t, MMA1_{t+1}, MMA2_{t+1}, MMA4_t, MMA5_t so that
+//    the next tile's products are queued while tile t's softmax runs.
 //    dQ is produced transposed so that TMEM lane = head-dim column: a warp's 32
 //    lanes then hold 32 consecutive floats of one query row, and the reduction
 //    into global dQ (red.global.add.f32) is one coalesced 128-byte access per
@@ -42,8 +44,10 @@
 //              and warpgroup 1 writes dK.
 //
 // Tensor memory (512 columns, f32 unless noted):
-//   [0,64) S^T buffer 0 (P^T bf16 in its first 32 columns)   [64,128) S^T buffer 1
-//   [128,192) dP^T   [192,256) dQ^T   [256,384) dV   [384,512) dK
+//   [0,128)   two 64-column buffers, one per tile parity: S^T_t, then P^T_t
+//             (bf16, first 32 columns), then dQ^T_t
+//   [128,256) two dP^T buffers, one per tile parity
+//   [256,384) dV   [384,512) dK
 //
 // Every wait is bounded, as in the forward kernel: a wait that runs out records
 // a status bit, the CTA drains what it has in flight and exits.
@@ -166,7 +170,7 @@ struct BwdLayout {
   static constexpr int NBAR = 1 + 2 * STAGES + 2 * 5 + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
   static constexpr uint32_t Q_TX = 2 * Q_TILE + 2 * BM * 4;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -297,16 +301,14 @@ __global__ void __launch_bounds__(384, 1)
         mma_scores(tmem + L::TM_DP, sv, sdo);
         umma_commit(&dp_full[0]);
       }
+      // Issue order per tile t: MMA3_t, then S and dP of tile t+1, then MMA4_t and
+      // MMA5_t.  The elementwise warps build P_t and dS_t while the tensor cores
+      // work on the queued products, so the pipe never waits on one tile's
+      // softmax before it can start the next tile's scores.
       for (int t = 0; ok && t < n_it; ++t) {
         const int st = t % STAGES, pb = t & 1;
         const uint32_t ph = (t >> 1) & 1;
         const int t1 = t + 1, st1 = t1 % STAGES;
-        if (t1 < n_it) {
-          if (!mbar_wait(&q_full[st1], (t1 / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q)) break;
-          tc_fence_after();
-          mma_scores(tmem + L::TM_S + (t1 & 1) * 64, sk, sq + st1 * L::Q_TILE);
-          umma_commit(&s_full[t1 & 1]);
-        }
         // MMA3: dV += P^T_t dO_t   (A = P^T bf16 in TMEM, B = dO_t MN-major)
         if (!mbar_wait(&p_full[pb], ph, wc, ST_BWD_TIMEOUT_P)) break;
         tc_fence_after();
@@ -318,6 +320,18 @@ __global__ void __launch_bounds__(384, 1)
             umma_ts(tmem + L::TM_DV, pt + kk * 8, bdesc, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
           }
         }
+        // S^T_{t+1} and dP^T_{t+1}.  Buffer (t+1)&1 last held dQ^T_{t-1}, which
+        // its warpgroup must have read out; dP buffer (t+1)&1 held dP^T_{t-1},
+        // read before dS_{t-1} was published (waited for at tile t-1).
+        if (t1 < n_it) {
+          if (!mbar_wait(&q_full[st1], (t1 / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q)) break;
+          if (t >= 1 && !mbar_wait(dq_empty, (t - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) break;
+          tc_fence_after();
+          mma_scores(tmem + L::TM_S + (t1 & 1) * 64, sk, sq + st1 * L::Q_TILE);
+          umma_commit(&s_full[t1 & 1]);
+          mma_scores(tmem + L::TM_DP + (t1 & 1) * 64, sv, sdo + st1 * L::Q_TILE);
+          umma_commit(&dp_full[t1 & 1]);
+        }
         // MMA4: dK += dS^T_t Q_t   (A = dS^T K-major in SMEM, B = Q_t MN-major)
         if (!mbar_wait(&ds_full[pb], ph, wc, ST_BWD_TIMEOUT_DS)) break;
         tc_fence_after();
@@ -328,19 +342,14 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t bdesc = sdesc_sw128(sq + st * L::Q_TILE + kk * 2048, L::Q_COLBLK, 1024);
           umma_ss(tmem + L::TM_DK, adesc, bdesc, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        // MMA2 of the next tile: dP^T_t has been read (dS_t is written)
-        if (t1 < n_it) {
-          mma_scores(tmem + L::TM_DP, sv, sdo + st1 * L::Q_TILE);
-          umma_commit(&dp_full[t1 & 1]);
-        }
-        // MMA5: dQ^T_t = K^T dS_t   (A = K MN-major, B = dS^T as [query][key] MN-major)
-        if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) break;
-        tc_fence_after();
+        // MMA5: dQ^T_t = K^T dS_t into S buffer pb (P_t there was consumed by
+        // MMA3_t, which the tensor cores finish first: they run in issue order).
+        // A = K MN-major, B = dS^T read as [query][key] MN-major.
 #pragma unroll
         for (int kk = 0; kk < L::BN / 16; ++kk) {
           const uint64_t adesc = sdesc_sw128(sk + kk * 2048, L::KV_COLBLK, 1024);
           const uint64_t bdesc = sdesc_sw128(ds_base + kk * 2048, L::DS_TILE, 1024);
-          umma_ss(tmem + L::TM_DQ, adesc, bdesc, IDESC_Q, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + L::TM_S + pb * 64, adesc, bdesc, IDESC_Q, kk > 0 ? 1u : 0u);
         }
         umma_commit(&dq_full[pb]);
         umma_commit(&q_empty[st]);
@@ -406,8 +415,8 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_after();
       uint32_t dpr[64];
-      FA_TMEM_LD32(lane_base + L::TM_DP + 0, dpr + 0);
-      FA_TMEM_LD32(lane_base + L::TM_DP + 32, dpr + 32);
+      FA_TMEM_LD32(lane_base + L::TM_DP + pb * 64 + 0, dpr + 0);
+      FA_TMEM_LD32(lane_base + L::TM_DP + pb * 64 + 32, dpr + 32);
       tmem_wait_ld();
       FA_REG_FENCE32(dpr + 0);
       FA_REG_FENCE32(dpr + 32);
@@ -438,8 +447,8 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_after();
       uint32_t qr[64];
-      FA_TMEM_LD32(lane_base + L::TM_DQ + 0, qr + 0);
-      FA_TMEM_LD32(lane_base + L::TM_DQ + 32, qr + 32);
+      FA_TMEM_LD32(s_col + 0, qr + 0);
+      FA_TMEM_LD32(s_col + 32, qr + 32);
       tmem_wait_ld();
       FA_REG_FENCE32(qr + 0);
       FA_REG_FENCE32(qr + 32);

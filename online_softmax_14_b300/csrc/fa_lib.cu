@@ -17,6 +17,7 @@
 #include "ptx.cuh"
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
+#include "fwd_tc2.cuh"
 #include "bwd_tc.cuh"
 
 namespace fa {
@@ -29,9 +30,9 @@ namespace {
 
 constexpr int kVersion = 200;  // 0.2.0
 constexpr int kMaxDevices = 64;
-constexpr int kStagesD128 = 3;
+constexpr int kStagesD128 = 2;
 constexpr int kStagesD64 = 4;
-constexpr int kStagesBwd = 2;
+constexpr int kStagesBwd = 3;
 
 thread_local char t_err[512] = "";
 std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};
@@ -79,12 +80,12 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaGetSymbolAddress(&addr, fa::g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
     s.status = static_cast<unsigned int*>(addr);
-    using L128 = fa::TcLayout<128, kStagesD128>;
-    using L64 = fa::TcLayout<64, kStagesD64>;
-    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<128, kStagesD128>,
+    using L128 = fa::Tc2Layout<128, kStagesD128>;
+    using L64 = fa::Tc2Layout<64, kStagesD64>;
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<128, kStagesD128>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L128::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
-    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<64, kStagesD64>,
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<64, kStagesD64>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L64::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
     if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -146,7 +147,7 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
 template <int D, int STAGES>
 fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len, int B,
                     int H, int N, float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
-  using L = fa::TcLayout<D, STAGES>;
+  using L = fa::Tc2Layout<D, STAGES>;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   fa_status s;
@@ -166,11 +167,11 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.load();
-  const long long blocks = static_cast<long long>(p.n_qt) * BH;
+  const long long blocks = static_cast<long long>((p.n_qt + 1) / 2) * BH;  // two query tiles per CTA
   if (blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
-  fa::fwd_bf16_tc_kernel<D, STAGES><<<static_cast<unsigned>(blocks), 256, L::BYTES, stream>>>(mq, mk, mv, p);
+  fa::fwd_bf16_tc2_kernel<D, STAGES><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc_kernel");
+  if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc2_kernel");
   return FA_OK;
 }
 

@@ -1,0 +1,383 @@
+// BFloat16 attention forward on the 5th-generation tensor cores (tcgen05, sm_103a),
+// two query tiles per CTA.
+//
+// One CTA computes query tiles 2p and 2p+1 (256 rows) of one (batch, head).  Both
+// tiles stream the same key/value tiles, so each K_j, V_j is loaded once for two
+// tiles.  Each tile keeps, per query row, the running max m, normaliser l and
+// accumulator acc of the online softmax ("The Flash Attention" page, online
+// recurrence panel):
+//     m_new = max(m, m'),  c = 2^(m - m_new),
+//     l <- l c + sum_j 2^(s_j - m_new),   acc <- acc c + sum_j 2^(s_j - m_new) V_j,
+//     O = acc / l once at the end, with O = 0 and lse = -inf when l = 0
+//     ("Flash attention and efficient attention: Worked examples", Cell D2).
+// Scores live in the base-2 domain, s = S * scale * log2(e), so every exponential
+// is one ex2.  The N x N score matrix never leaves the SM.
+//
+// Why two tiles: with one tile the tensor cores idle while that tile's softmax
+// runs, because the next product O += P V needs its result.  Here the MMA warp
+// issues S0_j, S1_j, then alternates PV0_j, S0_{j+1}, PV1_j, S1_{j+1}, ...: while
+// one warpgroup turns S into P, the tensor cores work on the other tile.
+//
+// Roles (384 threads; warps 10-11 only join the start and the end):
+//   warps 0-3   softmax of tile 0: thread r owns row r = tensor-memory lane r
+//   warps 4-7   softmax of tile 1
+//   warp 8      TMA producer: Q0, Q1 once, then K_j, V_j into a STAGES-deep ring
+//   warp 9      MMA issuer (one thread) and tensor-memory owner
+//
+// Tensor memory (512 columns, f32 unless noted):
+//   [0,128) S0, then P0 (bf16 pairs in its first 64 columns)   [128,256) S1 / P1
+//   [256,256+D) O0 accumulator   [256+D,256+2D) O1 accumulator
+// P_j aliases S_j: the tensor cores run in issue order, so S_{j+1}, issued after
+// PV_j, overwrites P_j only once PV_j has read it.
+//
+// Rescaling is lazy: a row's reference m moves only when a block's max exceeds it
+// by more than 8 (base 2).  l and acc always share the reference, so acc / l is
+// unchanged -- the cancellation of the Exercises page ("top and bottom both get
+// multiplied by e^-m") -- and the O round trip through tensor memory, together
+// with the wait for the previous PV product, happens only for blocks that move
+// the reference.  Terms stay below 2^8.
+#pragma once
+#include "ptx.cuh"
+#include "fwd_tc.cuh"  // status bits, TcParams
+
+namespace fa {
+
+template <int D, int STAGES>
+struct Tc2Layout {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int KB = D / 64;           // 64-element (128-byte) column blocks
+  static constexpr int COLBLK = 128 * 128;    // bytes of one 128-row column block
+  static constexpr int TILE = BM * D * 2;     // bytes of a Q, K or V tile
+  static constexpr int OFF_Q = 0;             // Q0, Q1
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE;
+  static constexpr int OFF_BAR = OFF_V + STAGES * TILE;
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D, TM_COLS = 512;
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(384, 1)
+    fwd_bf16_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+  using L = Tc2Layout<D, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + STAGES;
+  uint64_t* k_empty = v_full + STAGES;
+  uint64_t* v_empty = k_empty + STAGES;
+  uint64_t* s_full = v_empty + STAGES;  // [2], one per query tile
+  uint64_t* p_full = s_full + 2;        // [2]
+  uint64_t* o_done = p_full + 2;        // [2]
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Head-major order: consecutive CTAs share one head's K/V in L2; within a head
+  // the pairs with the most key tiles (causal) go first.
+  const int n_pair = (p.n_qt + 1) >> 1;
+  const int bh = static_cast<int>(blockIdx.x) / n_pair;
+  const int pr = n_pair - 1 - static_cast<int>(blockIdx.x) % n_pair;
+  const int b = bh / p.H;
+  const int q0 = pr * 2 * L::BM;  // first row of tile 0; tile 1 starts at q0 + 128
+  int kv_limit = p.N;
+  if (p.kv_len) kv_limit = min(p.N, max(0, p.kv_len[b]));
+  const int n_kv_all = (kv_limit + L::BN - 1) / L::BN;
+  // key tiles each query tile needs (0 for a tile entirely past N)
+  const int n_t0 = p.causal ? min(n_kv_all, 2 * pr + 1) : n_kv_all;
+  const int n_t1 = (2 * pr + 1 < p.n_qt) ? (p.causal ? min(n_kv_all, 2 * pr + 2) : n_kv_all) : 0;
+  const int n_max = max(n_t0, n_t1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, L::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+  constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
+
+  int k_issued = 0, v_issued = 0;  // K and V tiles whose loads the producer has issued
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0 && n_max > 0) {
+      const int nq = (n_t1 > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq * L::TILE);
+      for (int i = 0; i < nq; ++i)
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(smem + L::OFF_Q + i * L::TILE + kb * L::COLBLK, &tm_q, q_full, kb * 64, q0 + i * L::BM, bh);
+      for (int j = 0; j < n_max; ++j) {
+        const int st = j % STAGES;
+        const uint32_t ph = ((j / STAGES) - 1) & 1;
+        if (j >= STAGES && !mbar_wait(&k_empty[st], ph, wc, ST_TIMEOUT_EMPTY)) break;
+        if (p.inject == 1 && j == 1) break;  // test hook: starve the consumers
+        mbar_arrive_expect_tx(&k_full[st], L::TILE);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(smem + L::OFF_K + st * L::TILE + kb * L::COLBLK, &tm_k, &k_full[st], kb * 64, j * L::BN, bh);
+        k_issued = j + 1;
+        if (j >= STAGES && !mbar_wait(&v_empty[st], ph, wc, ST_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::TILE);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(smem + L::OFF_V + st * L::TILE + kb * L::COLBLK, &tm_v, &v_full[st], kb * 64, j * L::BN, bh);
+        v_issued = j + 1;
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer --
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, true);
+      const uint32_t sq = smem_u32(smem + L::OFF_Q);
+      const uint32_t sk = smem_u32(smem + L::OFF_K);
+      const uint32_t sv = smem_u32(smem + L::OFF_V);
+      auto issue_s = [&](uint32_t tm_s, uint32_t sq_i, uint64_t* bar, int j) {  // S_i = Q_i K_j^T
+        const int st = j % STAGES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
+          const uint64_t adesc = sdesc_sw128(sq_i + off, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(sk + st * L::TILE + off, 16, 1024);
+          umma_ss(tm_s, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar);
+      };
+      auto issue_pv = [&](uint32_t tm_o, uint32_t tm_p, uint64_t* bar, int j) {  // O_i += P_i V_j
+        const int st = j % STAGES;
+#pragma unroll
+        for (int kk = 0; kk < L::BN / 16; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(sv + st * L::TILE + kk * 2048, L::COLBLK, 1024);
+          umma_ts(tm_o, tm_p + kk * 8, bdesc, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar);
+      };
+      const uint32_t tS0 = tmem + L::TM_S0, tS1 = tmem + L::TM_S1;
+      const uint32_t tO0 = tmem + L::TM_O0, tO1 = tmem + L::TM_O1;
+      const uint32_t sq1 = sq + L::TILE;
+
+      bool ok = mbar_wait(q_full, 0, wc, ST_TIMEOUT_Q) && mbar_wait(&k_full[0], 0, wc, ST_TIMEOUT_K);
+      if (ok) {
+        tc_fence_after();
+        if (n_t0 > 0) issue_s(tS0, sq, &s_full[0], 0);
+        if (n_t1 > 0) issue_s(tS1, sq1, &s_full[1], 0);
+        umma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int st = j % STAGES, j1 = j + 1, st1 = j1 % STAGES;
+        // every tile that reads K_{j+1} or V_j waits for it once, before its first use
+        bool k1_ready = false, v_ready = false;
+        auto wait_v = [&]() -> bool {
+          if (v_ready) return true;
+          v_ready = mbar_wait(&v_full[st], (j / STAGES) & 1, wc, ST_TIMEOUT_V);
+          return v_ready;
+        };
+        auto wait_k1 = [&]() -> bool {
+          if (k1_ready) return true;
+          k1_ready = mbar_wait(&k_full[st1], (j1 / STAGES) & 1, wc, ST_TIMEOUT_K);
+          if (k1_ready) tc_fence_after();
+          return k1_ready;
+        };
+        // tile 0: PV0_j, then S0_{j+1}
+        if (j < n_t0) {
+          if (!wait_v() || !mbar_wait(&p_full[0], j & 1, wc, ST_TIMEOUT_P)) break;
+          tc_fence_after();
+          issue_pv(tO0, tS0, &o_done[0], j);
+        }
+        if (j1 < n_t0) {
+          if (!wait_k1()) break;
+          issue_s(tS0, sq, &s_full[0], j1);
+        }
+        // tile 1: PV1_j, then S1_{j+1}
+        if (j < n_t1) {
+          if (!wait_v() || !mbar_wait(&p_full[1], j & 1, wc, ST_TIMEOUT_P)) break;
+          tc_fence_after();
+          issue_pv(tO1, tS1, &o_done[1], j);
+        }
+        if (j1 < n_t1) {
+          if (!wait_k1()) break;
+          issue_s(tS1, sq1, &s_full[1], j1);
+        }
+        umma_commit(&v_empty[st]);                // V_j: read by every PV above
+        if (j1 < n_max) umma_commit(&k_empty[st1]);  // K_{j+1}: read by every S above
+      }
+      // nothing may be in flight on the tensor cores when the CTA frees TMEM
+      umma_commit(drain);
+      if (!mbar_wait_drain(drain, 0, DRAIN_NS)) atomicOr(p.status, ST_DRAIN);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------- softmax --
+    const int ti = warp >> 2;          // query tile 0 or 1 (warps 10-11 have no role)
+    const int r = threadIdx.x & 127;   // row in the tile == tensor-memory lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = lane_base + (ti ? L::TM_S1 : L::TM_S0);
+    const uint32_t o_col = lane_base + (ti ? L::TM_O1 : L::TM_O0);
+    const int qrow = q0 + ti * L::BM + r;
+    const int n_kv = ti ? n_t1 : n_t0;
+    const int qt0 = q0 + ti * L::BM;  // first row of this tile
+    const float sl = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      // tcgen05.ld/st are warp-collective: the whole warp goes on or stops together
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[ti], j & 1, wc, ST_TIMEOUT_S))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      FA_TMEM_LD32(s_col + 0, sr + 0);
+      FA_TMEM_LD32(s_col + 32, sr + 32);
+      FA_TMEM_LD32(s_col + 64, sr + 64);
+      FA_TMEM_LD32(s_col + 96, sr + 96);
+      tmem_wait_ld();
+      FA_REG_FENCE32(sr + 0);
+      FA_REG_FENCE32(sr + 32);
+      FA_REG_FENCE32(sr + 64);
+      FA_REG_FENCE32(sr + 96);
+
+      const int k0 = j * L::BN;
+      if (k0 + L::BN > kv_limit || (p.causal && k0 + L::BN - 1 > qt0)) {
+        int lim = kv_limit - k0;
+        if (p.causal) lim = min(lim, qrow - k0 + 1);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) sr[i] = __float_as_uint(-INFINITY);
+      }
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(sr[t]);
+#pragma unroll
+      for (int i = 8; i < 128; i += 8)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(mx8[t], __uint_as_float(sr[i + t]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_blk = mx * sl;
+      const float m_new = (m_blk > m + 8.f) ? m_blk : m;  // lazy reference move
+      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float c = ex2_approx(m - m_ref);               // 0 on the first block, 1 if unchanged
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P in quarters of 32 scores (16 packed columns) keeps register use low
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[32 * h + 2 * i]), sl, -m_ref));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[32 * h + 2 * i + 1]), sl, -m_ref));
+          rs4[i & 3] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        FA_TMEM_ST16(s_col + 16 * h, pk);
+      }
+      l = l * c + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+        // the accumulator holds blocks < j once PV_{j-1} has finished; o_done
+        // cannot run two phases ahead of this wait (PV_j needs this tile's P_j)
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[ti], (j - 1) & 1, wc, ST_TIMEOUT_O))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t orr[32];
+          FA_TMEM_LD32(o_col + cb * 32, orr);
+          tmem_wait_ld();
+          FA_REG_FENCE32(orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * c);
+          FA_TMEM_ST32(o_col + cb * 32, orr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[ti]);
+      m = m_new;
+    }
+
+    if (ok && n_kv > 0 && !__all_sync(0xffffffffu, mbar_wait(&o_done[ti], (n_kv - 1) & 1, wc, ST_TIMEOUT_O)))
+      ok = false;
+    if (ok && qt0 < p.N) {
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;  // guard: l = 0 -> zero vector
+      const size_t orow = (static_cast<size_t>(bh) * p.N + qrow) * D;
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t orr[32];
+        if (n_kv > 0) {
+          FA_TMEM_LD32(o_col + cb * 32, orr);
+          tmem_wait_ld();
+          FA_REG_FENCE32(orr);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = 0u;
+        }
+        uint32_t ob[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          ob[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+        if (qrow < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow + cb * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+        }
+      }
+      if (p.lse && qrow < p.N)
+        p.lse[static_cast<size_t>(bh) * p.N + qrow] = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8 && lane == 0 && n_max > 0 && *abort_flag) {
+    // an aborted CTA may not exit while copies it issued are still landing
+    bool ok = mbar_wait_drain(q_full, 0, DRAIN_NS);
+    for (int j = max(0, k_issued - STAGES); j < k_issued; ++j)
+      ok &= mbar_wait_drain(&k_full[j % STAGES], (j / STAGES) & 1, DRAIN_NS);
+    for (int j = max(0, v_issued - STAGES); j < v_issued; ++j)
+      ok &= mbar_wait_drain(&v_full[j % STAGES], (j / STAGES) & 1, DRAIN_NS);
+    if (!ok) atomicOr(p.status, ST_DRAIN);
+  }
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TM_COLS);
+  }
+}
+
+}  // namespace fa
