@@ -30,8 +30,8 @@ namespace {
 
 constexpr int kVersion = 200;  // 0.2.0
 constexpr int kMaxDevices = 64;
-constexpr int kStagesD128 = 2;
-constexpr int kStagesD64 = 4;
+constexpr int kSlotsD128 = 4;  // K/V ring slots of the forward (32 KB each at d = 128)
+constexpr int kSlotsD64 = 8;   // (16 KB each at d = 64)
 constexpr int kStagesBwd = 3;
 
 thread_local char t_err[512] = "";
@@ -80,12 +80,12 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaGetSymbolAddress(&addr, fa::g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
     s.status = static_cast<unsigned int*>(addr);
-    using L128 = fa::Tc2Layout<128, kStagesD128>;
-    using L64 = fa::Tc2Layout<64, kStagesD64>;
-    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<128, kStagesD128>,
+    using L128 = fa::Tc2Layout<128, kSlotsD128>;
+    using L64 = fa::Tc2Layout<64, kSlotsD64>;
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<128, kSlotsD128>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L128::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
-    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<64, kStagesD64>,
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<64, kSlotsD64>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L64::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
     if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -260,8 +260,8 @@ fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void
     if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "bf16 path serves d = 64 or 128 (got %d)", d);
     DeviceState* ds = nullptr;
     if ((s = device_state(&ds)) != FA_OK) return s;
-    if (d == 128) return launch_tc<128, kStagesD128>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
-    return launch_tc<64, kStagesD64>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
+    if (d == 128) return launch_tc<128, kSlotsD128>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
+    return launch_tc<64, kSlotsD64>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
   }
   if (dtype == FA_FP32) {
     if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 4)) != FA_OK) return s;

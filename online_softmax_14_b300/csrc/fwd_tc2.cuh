@@ -21,7 +21,7 @@
 // Roles (384 threads; warps 10-11 only join the start and the end):
 //   warps 0-3   softmax of tile 0: thread r owns row r = tensor-memory lane r
 //   warps 4-7   softmax of tile 1
-//   warp 8      TMA producer: Q0, Q1 once, then K_j, V_j into a STAGES-deep ring
+//   warp 8      TMA producer: Q0, Q1 once, then K_j, V_j through a ring of NS slots
 //   warp 9      MMA issuer (one thread) and tensor-memory owner
 //
 // Tensor memory (512 columns, f32 unless noted):
@@ -42,18 +42,20 @@
 
 namespace fa {
 
-template <int D, int STAGES>
+// NS = number of K/V slots: K_j and V_j stream through one ring of tile-sized
+// slots in the order K_0, V_0, K_1, V_1, ...; load number c (K_j: c = 2j, V_j:
+// c = 2j + 1) uses slot c % NS.
+template <int D, int NS>
 struct Tc2Layout {
   static constexpr int BM = 128, BN = 128;
   static constexpr int KB = D / 64;           // 64-element (128-byte) column blocks
   static constexpr int COLBLK = 128 * 128;    // bytes of one 128-row column block
   static constexpr int TILE = BM * D * 2;     // bytes of a Q, K or V tile
   static constexpr int OFF_Q = 0;             // Q0, Q1
-  static constexpr int OFF_K = 2 * TILE;
-  static constexpr int OFF_V = OFF_K + STAGES * TILE;
-  static constexpr int OFF_BAR = OFF_V + STAGES * TILE;
-  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 1;
+  static constexpr int OFF_KV = 2 * TILE;     // NS slots
+  static constexpr int OFF_BAR = OFF_KV + NS * TILE;
+  // barriers: q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 1 + 2 * NS + 6 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D, TM_COLS = 512;
@@ -61,20 +63,18 @@ struct Tc2Layout {
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, int STAGES>
+template <int D, int NS>
 __global__ void __launch_bounds__(384, 1)
     fwd_bf16_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
-  using L = Tc2Layout<D, STAGES>;
+  using L = Tc2Layout<D, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + STAGES;
-  uint64_t* k_empty = v_full + STAGES;
-  uint64_t* v_empty = k_empty + STAGES;
-  uint64_t* s_full = v_empty + STAGES;  // [2], one per query tile
+  uint64_t* kv_full = bars + 1;         // [NS]
+  uint64_t* kv_empty = kv_full + NS;    // [NS]
+  uint64_t* s_full = kv_empty + NS;     // [2], one per query tile
   uint64_t* p_full = s_full + 2;        // [2]
   uint64_t* o_done = p_full + 2;        // [2]
   uint64_t* drain = o_done + 2;
@@ -99,11 +99,9 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -112,6 +110,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8) = 0;
     fence_mbar_init();
   }
   if (warp == 8 && lane == 0) {
@@ -130,7 +129,9 @@ __global__ void __launch_bounds__(384, 1)
   const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
   constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
 
-  int k_issued = 0, v_issued = 0;  // K and V tiles whose loads the producer has issued
+  // K/V loads (c = 0, 1, ...) the producer has issued; kept in shared memory so
+  // that it holds no register in the other roles
+  volatile int* issued = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
     if (lane == 0 && n_max > 0) {
@@ -140,22 +141,17 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
           tma_load_3d(smem + L::OFF_Q + i * L::TILE + kb * L::COLBLK, &tm_q, q_full, kb * 64, q0 + i * L::BM, bh);
-      for (int j = 0; j < n_max; ++j) {
-        const int st = j % STAGES;
-        const uint32_t ph = ((j / STAGES) - 1) & 1;
-        if (j >= STAGES && !mbar_wait(&k_empty[st], ph, wc, ST_TIMEOUT_EMPTY)) break;
-        if (p.inject == 1 && j == 1) break;  // test hook: starve the consumers
-        mbar_arrive_expect_tx(&k_full[st], L::TILE);
+      for (int c = 0; c < 2 * n_max; ++c) {
+        const int slot = c % NS;
+        if (c >= NS && !mbar_wait(&kv_empty[slot], ((c / NS) - 1) & 1, wc, ST_TIMEOUT_EMPTY)) break;
+        if (p.inject == 1 && c == 2) break;  // test hook: starve the consumers after K_0, V_0
+        mbar_arrive_expect_tx(&kv_full[slot], L::TILE);
+        const CUtensorMap* src = (c & 1) ? &tm_v : &tm_k;
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(smem + L::OFF_K + st * L::TILE + kb * L::COLBLK, &tm_k, &k_full[st], kb * 64, j * L::BN, bh);
-        k_issued = j + 1;
-        if (j >= STAGES && !mbar_wait(&v_empty[st], ph, wc, ST_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::TILE);
-#pragma unroll
-        for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(smem + L::OFF_V + st * L::TILE + kb * L::COLBLK, &tm_v, &v_full[st], kb * 64, j * L::BN, bh);
-        v_issued = j + 1;
+          tma_load_3d(smem + L::OFF_KV + slot * L::TILE + kb * L::COLBLK, src, &kv_full[slot], kb * 64,
+                      (c >> 1) * L::BN, bh);
+        *issued = c + 1;
       }
     }
   } else if (warp == 9) {
@@ -164,51 +160,53 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, true);
       const uint32_t sq = smem_u32(smem + L::OFF_Q);
-      const uint32_t sk = smem_u32(smem + L::OFF_K);
-      const uint32_t sv = smem_u32(smem + L::OFF_V);
-      auto issue_s = [&](uint32_t tm_s, uint32_t sq_i, uint64_t* bar, int j) {  // S_i = Q_i K_j^T
-        const int st = j % STAGES;
+      const uint32_t skv = smem_u32(smem + L::OFF_KV);
+      // Descriptors of the tile bases; an operand at byte offset `off` from a
+      // base is that descriptor plus off >> 4 (the start-address field is the
+      // low 14 bits and every shared address here is below 2^18, so no carry).
+      const uint64_t dq_base = sdesc_sw128(sq, 16, 1024);
+      const uint64_t dk_base = sdesc_sw128(skv, 16, 1024);
+      const uint64_t dv_base = sdesc_sw128(skv, L::COLBLK, 1024);
+      auto issue_s = [&](uint32_t tm_s, uint32_t q_off, uint64_t* bar, int j) {  // S_i = Q_i K_j^T
+        const uint64_t ka = dk_base + ((((2 * j) % NS) * L::TILE) >> 4);
+        const uint64_t qa = dq_base + (q_off >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
-          const uint64_t adesc = sdesc_sw128(sq_i + off, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(sk + st * L::TILE + off, 16, 1024);
-          umma_ss(tm_s, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
+          umma_ss(tm_s, qa + off, ka + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar);
       };
       auto issue_pv = [&](uint32_t tm_o, uint32_t tm_p, uint64_t* bar, int j) {  // O_i += P_i V_j
-        const int st = j % STAGES;
+        const uint64_t va = dv_base + ((((2 * j + 1) % NS) * L::TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < L::BN / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(sv + st * L::TILE + kk * 2048, L::COLBLK, 1024);
-          umma_ts(tm_o, tm_p + kk * 8, bdesc, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < L::BN / 16; ++kk)
+          umma_ts(tm_o, tm_p + kk * 8, va + (kk * 2048 >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar);
       };
       const uint32_t tS0 = tmem + L::TM_S0, tS1 = tmem + L::TM_S1;
       const uint32_t tO0 = tmem + L::TM_O0, tO1 = tmem + L::TM_O1;
-      const uint32_t sq1 = sq + L::TILE;
 
-      bool ok = mbar_wait(q_full, 0, wc, ST_TIMEOUT_Q) && mbar_wait(&k_full[0], 0, wc, ST_TIMEOUT_K);
+      bool ok = mbar_wait(q_full, 0, wc, ST_TIMEOUT_Q) && mbar_wait(&kv_full[0], 0, wc, ST_TIMEOUT_K);
       if (ok) {
         tc_fence_after();
-        if (n_t0 > 0) issue_s(tS0, sq, &s_full[0], 0);
-        if (n_t1 > 0) issue_s(tS1, sq1, &s_full[1], 0);
-        umma_commit(&k_empty[0]);
+        if (n_t0 > 0) issue_s(tS0, 0, &s_full[0], 0);
+        if (n_t1 > 0) issue_s(tS1, L::TILE, &s_full[1], 0);
+        umma_commit(&kv_empty[0]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
-        const int st = j % STAGES, j1 = j + 1, st1 = j1 % STAGES;
+        const int j1 = j + 1;
+        const int cv = 2 * j + 1, ck = 2 * j1;  // load numbers of V_j and K_{j+1}
         // every tile that reads K_{j+1} or V_j waits for it once, before its first use
         bool k1_ready = false, v_ready = false;
         auto wait_v = [&]() -> bool {
           if (v_ready) return true;
-          v_ready = mbar_wait(&v_full[st], (j / STAGES) & 1, wc, ST_TIMEOUT_V);
+          v_ready = mbar_wait(&kv_full[cv % NS], (cv / NS) & 1, wc, ST_TIMEOUT_V);
           return v_ready;
         };
         auto wait_k1 = [&]() -> bool {
           if (k1_ready) return true;
-          k1_ready = mbar_wait(&k_full[st1], (j1 / STAGES) & 1, wc, ST_TIMEOUT_K);
+          k1_ready = mbar_wait(&kv_full[ck % NS], (ck / NS) & 1, wc, ST_TIMEOUT_K);
           if (k1_ready) tc_fence_after();
           return k1_ready;
         };
@@ -220,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (j1 < n_t0) {
           if (!wait_k1()) break;
-          issue_s(tS0, sq, &s_full[0], j1);
+          issue_s(tS0, 0, &s_full[0], j1);
         }
         // tile 1: PV1_j, then S1_{j+1}
         if (j < n_t1) {
@@ -230,10 +228,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (j1 < n_t1) {
           if (!wait_k1()) break;
-          issue_s(tS1, sq1, &s_full[1], j1);
+          issue_s(tS1, L::TILE, &s_full[1], j1);
         }
-        umma_commit(&v_empty[st]);                // V_j: read by every PV above
-        if (j1 < n_max) umma_commit(&k_empty[st1]);  // K_{j+1}: read by every S above
+        umma_commit(&kv_empty[cv % NS]);                 // V_j: read by every PV above
+        if (j1 < n_max) umma_commit(&kv_empty[ck % NS]);  // K_{j+1}: read by every S above
       }
       // nothing may be in flight on the tensor cores when the CTA frees TMEM
       umma_commit(drain);
@@ -278,28 +276,35 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) sr[i] = __float_as_uint(-INFINITY);
       }
+      // row max: 8 independent chains of three-input max
       float mx8[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(sr[t]);
+      for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1]));
 #pragma unroll
-      for (int i = 8; i < 128; i += 8)
+      for (int i = 16; i < 128; i += 16)
 #pragma unroll
-        for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(mx8[t], __uint_as_float(sr[i + t]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int t = 0; t < 8; ++t)
+          mx8[t] = fmax3(mx8[t], __uint_as_float(sr[i + 2 * t]), __uint_as_float(sr[i + 2 * t + 1]));
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float m_blk = mx * sl;
       const float m_new = (m_blk > m + 8.f) ? m_blk : m;  // lazy reference move
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float c = ex2_approx(m - m_ref);               // 0 on the first block, 1 if unchanged
+      // x = s * scale*log2(e) - m_ref two scores at a time (f32x2), p = 2^x, row
+      // sum in 4 independent chains; P in quarters of 32 scores (16 packed
+      // columns) keeps register use low
+      const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_ref, -m_ref);
       float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-      // P in quarters of 32 scores (16 packed columns) keeps register use low
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[32 * h + 2 * i]), sl, -m_ref));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[32 * h + 2 * i + 1]), sl, -m_ref));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[32 * h + 2 * i]), __uint_as_float(sr[32 * h + 2 * i + 1])),
+                           sl2, nm2),
+                    x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           rs4[i & 3] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
@@ -368,10 +373,9 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 8 && lane == 0 && n_max > 0 && *abort_flag) {
     // an aborted CTA may not exit while copies it issued are still landing
     bool ok = mbar_wait_drain(q_full, 0, DRAIN_NS);
-    for (int j = max(0, k_issued - STAGES); j < k_issued; ++j)
-      ok &= mbar_wait_drain(&k_full[j % STAGES], (j / STAGES) & 1, DRAIN_NS);
-    for (int j = max(0, v_issued - STAGES); j < v_issued; ++j)
-      ok &= mbar_wait_drain(&v_full[j % STAGES], (j / STAGES) & 1, DRAIN_NS);
+    const int n_iss = *issued;
+    for (int c = max(0, n_iss - NS); c < n_iss; ++c)
+      ok &= mbar_wait_drain(&kv_full[c % NS], (c / NS) & 1, DRAIN_NS);
     if (!ok) atomicOr(p.status, ST_DRAIN);
   }
   if (warp == 9) {
