@@ -26,7 +26,6 @@ exchange; value = all ranks' FLOPs / the slowest rank's time ("weak" scaling).
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -50,8 +49,14 @@ FALLBACK_BF16_TFLOPS = 1800.0  # used only when MEASURED_PEAKS.json is absent
 L2_BYTES = 126 * 1024 * 1024
 
 # DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture,
-# valid only for the kernel sources whose digest is recorded with it.
-NCU_TRAFFIC = {}  # {workload: {"bytes": int, "src_digest": str}}
+# valid only for the forward kernel sources whose digest is recorded with it.
+# The N=8192 launch was not captured itself: B=2 H=32 N=4096 (same kernel, half
+# the units) read 201,392,384 and wrote 48,744,448 bytes, and the traffic scales
+# with B*H*N*d (Q, K, V read once, O written once; K/V re-reads hit L2).
+NCU_TRAFFIC = {"bf16_causal_B2_H32_N8192_d128": {"bytes": 2 * (201392384 + 48744448),
+                                                 "src_digest": "81c5a7efb9979905",
+                                                 "how": "scaled x2 from an ncu capture of B=2 H=32 N=4096"}}
+FWD_SOURCES = ("fwd_tc.cuh", "ptx.cuh", "fa_lib.cu")
 
 
 def flops_per_step(w) -> float:
@@ -66,9 +71,10 @@ def bwd_flops(w) -> float:
 
 
 def kernel_src_digest() -> str:
+    """Digest of the sources the forward kernel is built from."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "online_softmax_14_b300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in FWD_SOURCES:
+        with open(os.path.join(ROOT, "online_softmax_14_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -314,6 +320,7 @@ def main():
     digest = kernel_src_digest()
     tr = NCU_TRAFFIC.get(w.name)
     traffic = tr["bytes"] if tr and tr["src_digest"] == digest else None
+    traffic_how = tr["how"] if traffic is not None else None
 
     line = {
         "metric": METRIC,
@@ -332,7 +339,7 @@ def main():
                    "seed": args.seed, "inputs_exceed_l2": in_bytes > L2_BYTES, "l2_flush": False,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_how,
                      "peak_source": f"{peak_src} bf16_tflops (burst)", "src_digest": digest},
         "e2e": e2e,
         "gpu_launches": args.steps,

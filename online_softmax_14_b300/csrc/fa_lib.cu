@@ -17,7 +17,6 @@
 #include "ptx.cuh"
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
-#include "fwd_tc2.cuh"
 #include "bwd_tc.cuh"
 
 namespace fa {
@@ -80,12 +79,12 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaGetSymbolAddress(&addr, fa::g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
     s.status = static_cast<unsigned int*>(addr);
-    using L128 = fa::Tc2Layout<128, kSlotsD128>;
-    using L64 = fa::Tc2Layout<64, kSlotsD64>;
-    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<128, kSlotsD128>,
+    using L128 = fa::TcLayout<128, kSlotsD128>;
+    using L64 = fa::TcLayout<64, kSlotsD64>;
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<128, kSlotsD128>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L128::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
-    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc2_kernel<64, kSlotsD64>,
+    if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<64, kSlotsD64>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L64::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
     if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -147,7 +146,7 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
 template <int D, int STAGES>
 fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len, int B,
                     int H, int N, float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
-  using L = fa::Tc2Layout<D, STAGES>;
+  using L = fa::TcLayout<D, STAGES>;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   fa_status s;
@@ -169,9 +168,9 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
   p.inject = g_inject.load();
   const long long blocks = static_cast<long long>((p.n_qt + 1) / 2) * BH;  // two query tiles per CTA
   if (blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
-  fa::fwd_bf16_tc2_kernel<D, STAGES><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, p);
+  fa::fwd_bf16_tc_kernel<D, STAGES><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc2_kernel");
+  if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc_kernel");
   return FA_OK;
 }
 
