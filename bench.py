@@ -64,6 +64,21 @@ def flops_per_step(w) -> float:
     return f / 2 if w.causal else f
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group):
+    a multi-GPU run is timed by its slowest rank."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Throughput of the whole job: every rank's FLOPs over the slowest rank's time."""
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def bwd_flops(w) -> float:
     """Five N x N x d products per head (S, dP, dV, dK, dQ), halved for causal."""
     f = 10.0 * w.B * w.H * w.N * w.N * w.d
@@ -239,6 +254,8 @@ def main():
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10, help="0 skips the end-to-end measurement")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="0 skips the CPU oracle baseline")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="--impl reference: approximate wall time of the whole run")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--bwd-steps", type=int, default=20,
                     help="timed steps of the forward + backward workload (0 skips it)")
@@ -301,14 +318,10 @@ def main():
         dist.barrier()
     fa.fa_check_device_error(stream)
     ms = e0.elapsed_time(e1) / args.steps
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
     f_step = flops_per_step(w)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
-    value = f_step * world / (ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(f_step, world, ms_max)
     achieved = f_step / (ms * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs -> device -> kernel -> host outputs
@@ -443,32 +456,66 @@ def run_e2e(args, w, inputs, step, q, k, v, kv, o, lse, stream, dev, dist, world
     torch.cuda.synchronize()
     fa.fa_check_device_error(stream)
     ms_e2e = e2.elapsed_time(e3) / args.e2e_steps
-    if dist:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e_value = f_step * world / (ms_e2e * 1e-3) / 1e12
+    ms_e2e = max_over_ranks(ms_e2e, dist, dev)
+    e2e_value = whole_job_tflops(f_step, world, ms_e2e)
     return {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)}
 
 
 def run_reference(args, w, rank, world):
-    """The float64 CPU oracle on the host cores, one whole (b, h) head per step."""
+    """The float64 CPU oracle on the host cores (rank 0 only).
+
+    Each step evaluates the oracle, as it stands, on a bounded sample of the
+    workload: the first R query rows of one (b, h) head (heads cycled), through
+    the oracle's ordinary whole-matrix path.  Under the causal mask those rows see
+    only keys < R, so the leading R x R block is exactly the first R rows of the
+    full problem; without it they see every key.  R is calibrated so that the
+    whole --warmup + --steps run takes about --ref-budget-s seconds.  FLOPs are
+    counted for the rows sampled, 4 * d * (visible keys) per row: the GPU
+    metric's unit.
+    """
     if rank != 0:
         return
+    import oracle
+
     inputs = make_workload(w, seed=args.seed)
-    heads = [((i * 7) % (w.B * w.H)) for i in range(args.warmup + args.steps)]
-    heads = [(bh // w.H, bh % w.H) for bh in heads]
-    for hh in heads[: args.warmup]:
-        oracle_heads(w, inputs, [hh], w.causal)
-    t = oracle_heads(w, inputs, heads[args.warmup:], w.causal)
-    per_head = flops_per_step(w) / (w.B * w.H)
-    value = per_head * args.steps / t / 1e12
+    kl = None if inputs["kv_len"] is None else [int(x) for x in inputs["kv_len"]]
+
+    def visible(b, i):
+        n = w.N if kl is None else min(w.N, kl[b])
+        return min(n, i + 1) if w.causal else n
+
+    def one_step(n_rows, k):
+        bh = (k * 7) % (w.B * w.H)
+        b, h = bh // w.H, bh % w.H
+        nk = n_rows if w.causal else w.N
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        t0 = time.perf_counter()
+        oracle.attention_fwd(inputs["q"][sl][:, :, :n_rows], inputs["k"][sl][:, :, :nk], inputs["v"][sl][:, :, :nk],
+                             inputs["scale"], causal=w.causal, kv_len=None if kl is None else [kl[b]])
+        dt = time.perf_counter() - t0
+        return dt, sum(4.0 * w.d * visible(b, i) for i in range(n_rows))
+
+    r0 = min(512, w.N)
+    t_cal, _ = one_step(r0, 0)
+    per_step_s = args.ref_budget_s / (args.steps + args.warmup)
+    grow = per_step_s / max(t_cal, 1e-6)
+    n_rows = int(r0 * (grow ** 0.5 if w.causal else grow))  # the work grows as R^2 (causal) or R
+    n_rows = max(64, min(w.N, n_rows))
+    for k in range(args.warmup):
+        one_step(n_rows, k + 1)
+    t_tot, f_tot = 0.0, 0.0
+    for k in range(args.steps):
+        dt, fl = one_step(n_rows, args.warmup + 1 + k)
+        t_tot += dt
+        f_tot += fl
+    value = f_tot / t_tot / 1e12
     cores = blas_threads()
-    sample = f"one whole (b,h) head of {w.name} per step, float64 NumPy with the full N x N scores"
+    sample = (f"the first {n_rows} query rows of one (b,h) head of {w.name} per step (heads cycled), "
+              f"float64 NumPy oracle with the full score block materialised")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_tot / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1))",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},

@@ -1,0 +1,87 @@
+"""The multi-GPU bench path on CPU: two gloo ranks, no GPU.
+
+The bench runs one replica of the workload per rank (the attention problems are
+independent, so there is no data exchange) and reports the whole job: every
+rank's FLOPs over the slowest rank's time.  These tests drive the helpers that
+do that across two real processes, and check that only rank 0 of the reference
+arm does any work.
+"""
+
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        local_ms = [2.0, 3.5][rank]  # rank 1 is the slower replica
+        ms_max = bench.max_over_ranks(local_ms, dist, "cpu")
+        value = bench.whole_job_tflops(1.0e12, world, ms_max)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"ms_max": ms_max, "value": value}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_report_slowest_time_and_total_work(tmp_path):
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)]
+    for r in res:
+        assert r["ms_max"] == 3.5                         # max over ranks, seen by every rank
+        assert r["value"] == pytest.approx(2 * 1.0e12 / 3.5e-3 / 1e12)  # both ranks' FLOPs / slowest time
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks(1.25, None, "cpu") == 1.25
+    assert bench.whole_job_tflops(2.0e12, 1, 1.0) == pytest.approx(2000.0)
+
+
+def _ref_rank_main(rank, world, out_dir):
+    sys.path.insert(0, ROOT)
+    import argparse
+    import contextlib
+    import io
+
+    import bench
+    from online_softmax_14_b300.inputs import Workload
+
+    w = Workload("tiny_causal", "bf16", 1, 2, 128, 64, True)
+    args = argparse.Namespace(seed=0, steps=2, warmup=1, ref_budget_s=1.0)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.run_reference(args, w, rank, world)
+    with open(os.path.join(out_dir, f"ref{rank}.txt"), "w") as f:
+        f.write(buf.getvalue())
+
+
+def test_reference_arm_runs_on_rank0_only(tmp_path):
+    mp.start_processes(_ref_rank_main, args=(2, str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    out0 = (tmp_path / "ref0.txt").read_text().strip().splitlines()
+    out1 = (tmp_path / "ref1.txt").read_text().strip()
+    assert out1 == ""                                     # other ranks exit without work
+    line = json.loads(out0[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
