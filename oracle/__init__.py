@@ -17,7 +17,9 @@ online
     A model of the tiled one-pass algorithm -- the running max / normaliser /
     accumulator recurrence and the block-state merge rule -- used to pin the
     definition against the pages' worked merges and to demonstrate that the
-    rescale factor is required.
+    rescale factor is required; and the same merge rule for normalised partial
+    results (O_p, lse_p), the definition the split-key merge kernel is checked
+    against.
 
 Every function states the passage of the source pages it follows.  Parity of every
 function here is pinned by ``tests/test_oracle_*.py`` against values the pages
@@ -31,4 +33,4 @@ from .attention import (  # noqa: F401
     attention_fwd_rows,
     score_matrix,
 )
-from .online import merge_states, online_attention, online_row  # noqa: F401
+from .online import merge_outputs, merge_states, online_attention, online_row  # noqa: F401

@@ -131,3 +131,32 @@ def online_attention(q, k, v, scale: float, causal: bool = False, kv_len=None,
                 o[b, h, i], lse[b, h, i], _, _ = online_row(s, v[b, h], block_size,
                                                              drop_rescale=drop_rescale)
     return o, lse
+
+
+def merge_outputs(o_parts, lse_parts):
+    """Merge normalised partial results computed over disjoint key sets.
+
+    A part with output O_p (already divided by its own normaliser) and
+    log-normaliser lse_p is the block state (m = lse_p, l = 1, O~ = O_p): dividing
+    O~ by l gives O_p and m + ln l gives lse_p.  The generic merge rule of the
+    Exercises page (two-block and three-block merges) then applies unchanged:
+        m = max_p lse_p,   f_p = e^(lse_p - m),   l = sum_p f_p,
+        O = sum_p f_p O_p / l,   lse = m + ln l.
+    Parts with lse_p = -inf (no visible key) carry zero weight; if every part
+    has lse = -inf the result is O = 0 and lse = -inf (Worked examples, Cell D2).
+
+    o_parts: [P, ..., dv]; lse_parts: [P, ...].  Returns (O [..., dv], lse [...])
+    in float64.
+    """
+    o = np.asarray(o_parts, dtype=np.float64)
+    lse = np.asarray(lse_parts, dtype=np.float64)
+    m = lse.max(axis=0)
+    m_ref = np.where(np.isneginf(m), 0.0, m)
+    f = np.exp(lse - m_ref[None])
+    l = f.sum(axis=0)
+    num = (f[..., None] * o).sum(axis=0)
+    safe = np.where(l > 0, l, 1.0)
+    out = np.where((l > 0)[..., None], num / safe[..., None], 0.0)
+    with np.errstate(divide="ignore"):
+        out_lse = np.where(l > 0, m_ref + np.log(safe), NEG_INF)
+    return out, out_lse
