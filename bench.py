@@ -259,6 +259,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--bwd-steps", type=int, default=20,
                     help="timed steps of the forward + backward workload (0 skips it)")
+    ap.add_argument("--merge-steps", type=int, default=20,
+                    help="timed steps of the split-key merge (0 skips it)")
     ap.add_argument("--bwd-shape", default=None,
                     help="B,H,N: a custom causal d=128 forward + backward workload (profiling runs)")
     args = ap.parse_args()
@@ -361,6 +363,8 @@ def main():
     }
     if args.bwd_steps > 0 and not args.shape:
         line["fwd_bwd"] = run_fwd_bwd(args, fa, dev, stream, dist)
+    if args.merge_steps > 0 and not args.shape:
+        line["merge"] = run_merge(args, fa, w, dev, stream, peaks)
     if rank == 0 and world == 1 and args.cpu_budget_s > 0:
         line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_budget_s)
     if rank == 0:
@@ -417,6 +421,42 @@ def run_fwd_bwd(args, fa, dev, stream, dist):
             "fwd_bwd_tflops": round((ff + fb) / (ms_f + ms_b) / 1e9, 2),
             "flops": {"fwd": ff, "bwd": fb, "bwd_formula": "10*B*H*N^2*d, halved for causal"},
             "gpu_launches_per_bwd": 2}
+
+
+def run_merge(args, fa, w, dev, stream, peaks, n_parts=4):
+    """Split-key merge of n_parts bf16 partial results of the workload's shape
+    (as a split-key forward over n_parts key ranges would produce them), timed
+    with CUDA events on the launching stream.  Device-memory bound: the
+    algorithmic bytes are every part's O and lse read once and the merged O and
+    lse written once."""
+    g = torch.Generator(device="cpu").manual_seed(args.seed)
+    R = w.B * w.H * w.N
+    o_p = torch.randn(n_parts, w.B, w.H, w.N, w.d, generator=g).to(torch.bfloat16).to(dev)
+    l_p = (torch.randn(n_parts, w.B, w.H, w.N, generator=g) * 4).to(dev)
+    o = torch.empty(o_p.shape[1:], dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(l_p.shape[1:], dtype=torch.float32, device=dev)
+
+    def step():
+        fa.fa_merge(fa.FA_BF16, o_p, l_p, n_parts, o, lse, w.B, w.H, w.N, w.d, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.merge_steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error(stream)
+    ms = a.elapsed_time(b) / args.merge_steps
+    nbytes = n_parts * R * (w.d * 2 + 4) + R * (w.d * 2 + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", 6400.0))
+    return {"workload": f"{n_parts} bf16 parts of {w.name}", "steps": args.merge_steps, "ms": round(ms, 4),
+            "bytes_per_call": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4)}}
 
 
 def run_e2e(args, w, inputs, step, q, k, v, kv, o, lse, stream, dev, dist, world, fa):

@@ -116,6 +116,27 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * fa_merge -- combine partial attention results computed over disjoint key
+ * sets (split-key attention).  Part p gives, for every query row, an output O_p
+ * already divided by its own normaliser and that normaliser's natural log lse_p
+ * (what fa_fwd returns for the keys it was given).  The merge is the generic
+ * rule of "Exercises -- Flash attention and efficient attention" (two- and
+ * three-block merges), applied to the states (m = lse_p, l = 1, O~ = O_p):
+ *     m = max_p lse_p,  f_p = e^(lse_p - m),  O = sum_p f_p O_p / sum_p f_p,
+ *     lse = m + ln sum_p f_p.
+ * A part with lse_p = -inf carries no weight; if all are -inf, O = 0 and
+ * lse = -inf.
+ *   dtype     : FA_BF16 or FA_FP32, the element type of o_parts and o.
+ *   o_parts   : DEVICE, [n_parts][B][H][N][d], contiguous, element-aligned.
+ *   lse_parts : DEVICE float*, [n_parts][B][H][N].
+ *   o         : DEVICE, [B][H][N][d], written.
+ *   lse       : DEVICE float*, [B][H][N], or NULL (not written).
+ *   1 <= n_parts <= 4096; 1 <= d <= 256 (else FA_ERR_UNSUPPORTED).
+ */
+fa_status fa_merge(int dtype, const void* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int B,
+                   int H, int N, int d, void* stream);
+
+/*
  * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
  * The source pages have no counterpart: it exists only because of how some
  * callers manage memory.  A caller that cannot call cudaMalloc when it needs a

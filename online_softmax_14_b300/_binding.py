@@ -51,6 +51,8 @@ _lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _
 _lib.fa_bwd.restype = _i
 _lib.fa_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_bwd_ex.restype = _i
+_lib.fa_merge.argtypes = [_i, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp]
+_lib.fa_merge.restype = _i
 _lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_bwd_noalloc.restype = _i
 FA_BWD_NOALLOC_MAX_ROWS = 524288
@@ -133,6 +135,28 @@ def fa_bwd_ex(q, k, v, o, do, lse, kv_len, dq, dk, dv, workspace, workspace_byte
     _check(_lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(kv_len), _ptr(dq),
                           _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale),
                           int(bool(causal)), _stream(stream)))
+
+
+def fa_merge(dtype, o_parts, lse_parts, n_parts, o, lse, B, H, N, d, stream=None) -> None:
+    _check(_lib.fa_merge(int(dtype), _ptr(o_parts), _ptr(lse_parts), int(n_parts), _ptr(o), _ptr(lse), B, H, N, d,
+                         _stream(stream)))
+
+
+def attention_merge(o_parts, lse_parts, stream=None):
+    """O, lse of the merge of partial results: o_parts [P, B, H, N, d] (bf16 or
+    fp32), lse_parts [P, B, H, N] fp32, CUDA tensors.  Allocates the outputs with
+    PyTorch and runs ``fa_merge``."""
+    if o_parts.dtype not in (torch.bfloat16, torch.float32) or lse_parts.dtype != torch.float32:
+        raise TypeError("o_parts must be bf16 or fp32 and lse_parts fp32")
+    if not (o_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()
+            and lse_parts.shape == o_parts.shape[:-1]):
+        raise ValueError("o_parts [P, B, H, N, d] and lse_parts [P, B, H, N] must be contiguous CUDA tensors")
+    P, B, H, N, d = o_parts.shape
+    o = torch.empty(o_parts.shape[1:], dtype=o_parts.dtype, device=o_parts.device)
+    lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    fa_merge(FA_BF16 if o_parts.dtype == torch.bfloat16 else FA_FP32, o_parts, lse_parts, P, o, lse, B, H, N, d,
+             stream)
+    return o, lse
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, stream=None) -> None:

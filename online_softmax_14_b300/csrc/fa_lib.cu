@@ -18,6 +18,7 @@
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
 #include "bwd_tc.cuh"
+#include "merge.cuh"
 
 namespace fa {
 // Status word of the current device: kernels OR their timeout codes into it;
@@ -326,6 +327,66 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream) {
   return fa_bwd_ex(q, k, v, o, dO, lse, nullptr, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
                    stream);
+}
+
+fa_status fa_merge(int dtype, const void* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int B,
+                   int H, int N, int d, void* stream) {
+  t_err[0] = '\0';
+  if (!o_parts || !lse_parts || !o) return fail(FA_ERR_INVALID, "o_parts, lse_parts and o must be non-null");
+  if (B < 1 || H < 1 || N < 1 || d < 1 || n_parts < 1)
+    return fail(FA_ERR_INVALID, "sizes must be >= 1 (B=%d H=%d N=%d d=%d n_parts=%d)", B, H, N, d, n_parts);
+  if (d > 256) return fail(FA_ERR_UNSUPPORTED, "merge serves d <= 256 (got %d)", d);
+  if (n_parts > 4096) return fail(FA_ERR_UNSUPPORTED, "merge serves at most 4096 parts (got %d)", n_parts);
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID, "unknown dtype %d", dtype);
+  const uintptr_t al = (dtype == FA_FP32) ? 4 : 2;
+  if (!aligned(o_parts, al) || !aligned(o, al) || !aligned(lse_parts, 4) || (lse && !aligned(lse, 4)))
+    return fail(FA_ERR_INVALID, "misaligned pointer (o_parts/o need %d bytes, lse 4)", (int)al);
+  const long long R = static_cast<long long>(B) * H * N;
+  const long long blocks = (R + fa::MERGE_ROWS - 1) / fa::MERGE_ROWS;
+  if (R > (1ll << 40) || blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "problem too large");
+  fa_status s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(&ds)) != FA_OK) return s;
+  fa::MergeParams p{o_parts, lse_parts, o, lse, R, n_parts, d};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 block(fa::MERGE_ROWS * 32);
+  // 16-byte vectors when a row is 16, 32, ..., 512 bytes and both tensors are 16-byte aligned
+  const int row_bytes = d * static_cast<int>(al);
+  const int lpr = row_bytes / 16;
+  if (row_bytes % 16 == 0 && lpr >= 1 && lpr <= 32 && (lpr & (lpr - 1)) == 0 && aligned(o_parts, 16) &&
+      aligned(o, 16)) {
+    const long long rows_per_cta = static_cast<long long>(fa::MERGE_ROWS) * (32 / lpr);
+    const dim3 vgrid(static_cast<unsigned>((R + rows_per_cta - 1) / rows_per_cta));
+#define FA_MERGE_VEC(T)                                                                            \
+  switch (lpr) {                                                                                   \
+    case 1: fa::merge_vec_kernel<T, 1><<<vgrid, block, 0, st>>>(p); break;                         \
+    case 2: fa::merge_vec_kernel<T, 2><<<vgrid, block, 0, st>>>(p); break;                         \
+    case 4: fa::merge_vec_kernel<T, 4><<<vgrid, block, 0, st>>>(p); break;                         \
+    case 8: fa::merge_vec_kernel<T, 8><<<vgrid, block, 0, st>>>(p); break;                         \
+    case 16: fa::merge_vec_kernel<T, 16><<<vgrid, block, 0, st>>>(p); break;                       \
+    default: fa::merge_vec_kernel<T, 32><<<vgrid, block, 0, st>>>(p); break;                       \
+  }
+    if (dtype == FA_FP32) {
+      FA_MERGE_VEC(float)
+    } else {
+      FA_MERGE_VEC(__nv_bfloat16)
+    }
+#undef FA_MERGE_VEC
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch merge_vec_kernel");
+    return FA_OK;
+  }
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (dtype == FA_FP32) {
+    if (d <= 128) fa::merge_kernel<float, 4><<<grid, block, 0, st>>>(p);
+    else fa::merge_kernel<float, 8><<<grid, block, 0, st>>>(p);
+  } else {
+    if (d <= 128) fa::merge_kernel<__nv_bfloat16, 4><<<grid, block, 0, st>>>(p);
+    else fa::merge_kernel<__nv_bfloat16, 8><<<grid, block, 0, st>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch merge_kernel");
+  return FA_OK;
 }
 
 const char* fa_status_string(int status) {

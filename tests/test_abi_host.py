@@ -121,3 +121,24 @@ def test_bwd_workspace_size():
 def test_bwd_host_validation(kw, status):
     assert _bwd(**kw) == status
     assert fa.fa_last_error_string() != ""
+
+
+def _merge(dtype=0, op=P, lp=P, n=2, o=P, lse=None, Bs=1, H=1, N=16, d=64):
+    return B.fa_status_raw("fa_merge", dtype, op, lp, n, o, lse, Bs, H, N, d, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(op=None), B.FA_ERR_INVALID),
+    (dict(lp=None), B.FA_ERR_INVALID),
+    (dict(o=None), B.FA_ERR_INVALID),
+    (dict(n=0), B.FA_ERR_INVALID),
+    (dict(N=0), B.FA_ERR_INVALID),
+    (dict(dtype=5), B.FA_ERR_INVALID),
+    (dict(dtype=1, op=P + 2), B.FA_ERR_INVALID),   # fp32 parts need 4-byte alignment
+    (dict(lp=P + 2), B.FA_ERR_INVALID),
+    (dict(d=257), B.FA_ERR_UNSUPPORTED),
+    (dict(n=4097), B.FA_ERR_UNSUPPORTED),
+])
+def test_merge_host_validation(kw, status):
+    assert _merge(**kw) == status
+    assert fa.fa_last_error_string() != ""
