@@ -28,6 +28,7 @@ print, closed forms, invariants and high-precision brute force.
 
 from .attention import (  # noqa: F401
     NEG_INF,
+    STRICT,
     attention_bwd,
     attention_fwd,
     attention_fwd_rows,

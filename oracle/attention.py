@@ -26,7 +26,8 @@ Sources (page title, then section):
     path forms the full n x n score matrix, as this module does.
 
 Readings where the pages are silent (each is listed in the design notes):
-  * causal is inclusive (j <= i) with queries and keys indexed alike;
+  * causal is inclusive (j <= i) with queries and keys indexed alike; the
+    strictly causal mode (j < i) is Cell D2's setting;
   * key padding: keys j >= kv_len[b] are masked for every head and query of batch
     b (the pages do not mention padding; it is the same -inf mask as Cell D);
   * lse is the natural log of sum_j exp(S_ij) over visible keys, i.e. m + ln l,
@@ -63,16 +64,34 @@ def score_matrix(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
     return scale * (q @ k.T)
 
 
-def visible_mask(nq: int, nk: int, causal: bool, kv_len: int | None) -> np.ndarray:
+STRICT = 2  # causal mode: a query may not attend to itself
+
+
+def key_visible(j, i, causal) -> np.ndarray:
+    """Causal rule for key index j and query index i (arrays broadcast).
+
+    causal = 0/False: every key.  1/True (Worked examples, Cell D): keys j <= i,
+    the token sees itself.  2 (Cell D2's "strictly causal setup"): keys j < i
+    only, so query 0 sees no key at all.
+    """
+    j = np.asarray(j)
+    if not causal:
+        return np.ones(np.broadcast(j, np.asarray(i)).shape, dtype=bool)
+    if causal == STRICT:
+        return j < i
+    return j <= i
+
+
+def visible_mask(nq: int, nk: int, causal, kv_len: int | None) -> np.ndarray:
     """Boolean [Nq, Nk]: True where query i may attend to key j.
 
-    Causal (Worked examples, Cell D): key j is visible to query i iff j <= i.
-    Key padding (a reading; the pages have no padding): key j is visible iff
-    j < kv_len.
+    Causal (Worked examples, Cell D): key j is visible to query i iff j <= i;
+    strictly causal (Cell D2) iff j < i.  Key padding (a reading; the pages have
+    no padding): key j is visible iff j < kv_len.
     """
     vis = np.ones((nq, nk), dtype=bool)
     if causal:
-        vis &= np.arange(nk)[None, :] <= np.arange(nq)[:, None]
+        vis &= key_visible(np.arange(nk)[None, :], np.arange(nq)[:, None], causal)
     if kv_len is not None:
         vis &= np.arange(nk)[None, :] < int(kv_len)
     return vis
@@ -131,8 +150,9 @@ def attention_fwd(q, k, v, scale: float, causal: bool = False, kv_len=None):
     """Exact attention forward over every (b, h).
 
     q, k: [B, H, N, dk]; v: [B, H, N, dv] (any float type, converted exactly to
-    float64); scale: the score multiplier (1/sqrt(dk) in the pages); causal:
-    inclusive causal mask; kv_len: None or B integers in [0, N].
+    float64); scale: the score multiplier (1/sqrt(dk) in the pages); causal: 0
+    (none), 1 (inclusive, j <= i) or 2 (strict, j < i); kv_len: None or B
+    integers in [0, N].
 
     Returns (O [B, H, N, dv] float64, lse [B, H, N] float64).
     """
@@ -165,7 +185,7 @@ def attention_fwd_rows(q, k, v, scale: float, causal: bool, kv_len, rows):
         s = score_matrix(qi, kk, scale)
         vis = np.ones((1, nk), dtype=bool)
         if causal:
-            vis &= np.arange(nk)[None, :] <= i
+            vis &= key_visible(np.arange(nk)[None, :], i, causal)
         if kv_len is not None:
             vis &= np.arange(nk)[None, :] < int(kv_len[b])
         s = apply_mask(s, vis)

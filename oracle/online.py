@@ -113,7 +113,7 @@ def online_attention(q, k, v, scale: float, causal: bool = False, kv_len=None,
     Same arguments and results as ``attention.attention_fwd``.  The score row is
     formed one query at a time and consumed block by block.
     """
-    from .attention import _f64
+    from .attention import _f64, key_visible
 
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, _ = q.shape
@@ -125,7 +125,7 @@ def online_attention(q, k, v, scale: float, causal: bool = False, kv_len=None,
                 s = scale * (k[b, h] @ q[b, h, i])
                 j = np.arange(N)
                 if causal:
-                    s = np.where(j <= i, s, NEG_INF)
+                    s = np.where(key_visible(j, i, causal), s, NEG_INF)
                 if kv_len is not None:
                     s = np.where(j < int(kv_len[b]), s, NEG_INF)
                 o[b, h, i], lse[b, h, i], _, _ = online_row(s, v[b, h], block_size,

@@ -13,6 +13,7 @@ CASES = [
     (1, 2, 6, 4, True, None),
     (2, 1, 7, 2, False, [3, 7]),
     (2, 1, 6, 4, True, [0, 5]),
+    (1, 2, 6, 3, 2, None),           # strictly causal (Worked examples, Cell D2's setting)
 ]
 
 

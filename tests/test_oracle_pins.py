@@ -99,3 +99,28 @@ def test_bf16_inputs_convert_exactly():
     a = _f64(t)
     assert a.dtype == np.float64
     assert np.array_equal(a, t.float().numpy().astype(np.float64))
+
+
+def test_strictly_causal_cell_d2():
+    """Worked examples, Cell D2: in a strictly causal setup query 0 has no earlier
+    token, every score is -inf, l = 0, and the output is the zero vector (lse is
+    -inf).  Every later query i attends exactly to keys 0 .. i-1."""
+    rng = np.random.default_rng(21)
+    N, d = 6, 3
+    q, k, v = (rng.standard_normal((1, 1, N, d)) for _ in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 0.5, causal=oracle.STRICT)
+    assert np.array_equal(o[0, 0, 0], np.zeros(d)) and np.isneginf(lse[0, 0, 0])
+    for i in range(1, N):
+        # the same row computed without a mask over the i earlier keys only
+        oi, li = oracle.attention_fwd(q[:, :, i:i + 1], k[:, :, :i], v[:, :, :i], 0.5)
+        assert np.allclose(o[0, 0, i], oi[0, 0, 0], rtol=1e-14) and lse[0, 0, i] == pytest.approx(li[0, 0, 0])
+    # inclusive causal differs from strict exactly by the diagonal key
+    o1, _ = oracle.attention_fwd(q, k, v, 0.5, causal=True)
+    assert not np.allclose(o1[0, 0, 1:], o[0, 0, 1:])
+    # the recurrence model and the backward agree with the definition in this mode
+    oo, lo = online.online_attention(q, k, v, 0.5, causal=oracle.STRICT, block_size=2)
+    assert np.allclose(oo, o, atol=1e-14) and np.array_equal(np.isneginf(lo), np.isneginf(lse))
+    do = rng.standard_normal(q.shape)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.5, causal=oracle.STRICT)
+    assert np.all(dq[0, 0, 0] == 0)                       # query 0 took part in nothing
+    assert np.all(dk[0, 0, N - 1] == 0) and np.all(dv[0, 0, N - 1] == 0)  # the last key is seen by no query
