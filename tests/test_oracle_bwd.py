@@ -56,8 +56,8 @@ def test_bwd_matches_autograd(case):
     tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
     s = scale * tq @ tk.transpose(-1, -2)
     vis = torch.ones(B, 1, N, N, dtype=torch.bool)
-    if causal:
-        vis &= torch.ones(N, N, dtype=torch.bool).tril()
+    if causal:  # inclusive (j <= i) or, for causal = 2, strict (j < i)
+        vis &= torch.ones(N, N, dtype=torch.bool).tril(-1 if causal == 2 else 0)
     if kv is not None:
         for b in range(B):
             vis[b, :, :, kv[b]:] = False
