@@ -57,7 +57,11 @@ typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
  *   lse     : float*, [B, H, N] or NULL (then not written); natural-log
  *             log-sum-exp of each row's scaled, masked scores.
  *   d       : 64 or 128 (else FA_ERR_UNSUPPORTED).
- *   causal  : nonzero -> query i attends to keys j <= i.
+ *   causal  : 0 -> no mask; 1 -> query i attends to keys j <= i ("Flash
+ *             attention and efficient attention: Worked examples", Cell D);
+ *             2 -> keys j < i only, the strictly causal setup of Cell D2, where
+ *             query 0 sees no key (O = 0, lse = -inf).  Other values return
+ *             FA_ERR_INVALID.  The same codes apply to every call below.
  * Runs on the tensor cores (tcgen05.mma, accumulators in tensor memory,
  * operands staged by TMA); the N x N scores never reach device memory.
  */

@@ -84,6 +84,16 @@ def _stream(stream):
     return int(stream)
 
 
+def _causal(causal) -> int:
+    """0/False: no mask; 1/True: key j visible to query i iff j <= i; 2 or
+    "strict": iff j < i (a query does not see its own key)."""
+    if causal == "strict":
+        return 2
+    if isinstance(causal, bool) or causal is None:
+        return int(bool(causal))
+    return int(causal)
+
+
 def _check(status: int):
     if status != FA_OK:
         raise FaError(status, _lib.fa_last_error_string().decode())
@@ -110,13 +120,13 @@ def fa_debug_inject(code: int) -> None:
 
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None) -> None:
-    _check(_lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
+    _check(_lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), _causal(causal),
                        _stream(stream)))
 
 
 def fa_fwd_ex(dtype, q, k, v, o, lse, kv_len, B, H, N, d, scale, causal, stream=None) -> None:
     _check(_lib.fa_fwd_ex(int(dtype), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(kv_len), B, H, N, d,
-                          float(scale), int(bool(causal)), _stream(stream)))
+                          float(scale), _causal(causal), _stream(stream)))
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:
@@ -126,7 +136,7 @@ def fa_bwd_workspace_size(B, H, N, d) -> int:
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
            stream=None) -> None:
     _check(_lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                       _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale), int(bool(causal)),
+                       _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale), _causal(causal),
                        _stream(stream)))
 
 
@@ -134,7 +144,7 @@ def fa_bwd_ex(q, k, v, o, do, lse, kv_len, dq, dk, dv, workspace, workspace_byte
               stream=None) -> None:
     _check(_lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(kv_len), _ptr(dq),
                           _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N, d, float(scale),
-                          int(bool(causal)), _stream(stream)))
+                          _causal(causal), _stream(stream)))
 
 
 def fa_merge(dtype, o_parts, lse_parts, n_parts, o, lse, B, H, N, d, stream=None) -> None:
@@ -163,7 +173,7 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, s
     """fa_bwd without a workspace argument: the library uses its own fixed
     device scratch (for callers that cannot allocate device memory)."""
     _check(_lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _stream(stream)))
+                               _ptr(dv), B, H, N, d, float(scale), _causal(causal), _stream(stream)))
 
 
 def fa_check_device_error(stream=None) -> None:

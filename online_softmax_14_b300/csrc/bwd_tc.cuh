@@ -141,7 +141,7 @@ struct BwdParams {
   int n_kt;                 // key tiles per head
   float scale;              // score multiplier
   float scale_log2;         // scale * log2(e)
-  int causal;
+  int causal;               // 0 none, 1 key k visible iff k <= row, 2 iff k < row
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -387,8 +387,9 @@ __global__ void __launch_bounds__(384, 1)
       FA_REG_FENCE32(sr + 32);
       const float* lse2 = reinterpret_cast<const float*>(smem + L::OFF_LSE + st * L::BM * 4);
       const float* dd = reinterpret_cast<const float*>(smem + L::OFF_DD + st * L::BM * 4);
-      // causal: key k0 + r is visible to query q0 + j iff j >= r - (q0 - k0)
-      const int jmin = p.causal ? r - (q0 - k0) : -1;
+      // causal: key k0 + r is visible to query q0 + j iff j >= r - (q0 - k0), one
+      // later in the strict mode (a query does not see its own key)
+      const int jmin = p.causal ? r - (q0 - k0) + (p.causal == 2 ? 1 : 0) : -1;
       float pr[64];
 #pragma unroll
       for (int j4 = 0; j4 < 64; j4 += 4) {

@@ -129,6 +129,12 @@ fa_status make_map(CUtensorMap* m, const void* base, int d, int N, int BH, const
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// causal: 0 none, 1 key j visible to query i iff j <= i, 2 iff j < i (strict)
+fa_status check_causal(int causal) {
+  if (causal < 0 || causal > 2) return fail(FA_ERR_INVALID, "causal must be 0, 1 or 2 (got %d)", causal);
+  return FA_OK;
+}
+
 fa_status check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
                        int N, int d, float scale, uintptr_t align) {
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID, "q, k, v and o must be non-null device pointers");
@@ -163,7 +169,8 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
   p.N = N;
   p.n_qt = (N + 127) / 128;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.causal = causal ? 1 : 0;
+  p.causal = causal;
+  p.cdiag = (causal == 2) ? 0 : 1;
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.load();
@@ -238,7 +245,7 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.n_kt = static_cast<int>(n_kt);
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.causal = causal ? 1 : 0;
+  p.causal = causal;
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, p);
@@ -254,6 +261,7 @@ fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void
                     const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream) {
   t_err[0] = '\0';
   fa_status s;
+  if ((s = check_causal(causal)) != FA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == FA_BF16) {
     if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
@@ -282,7 +290,7 @@ fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void
     p.d = d;
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.causal = causal ? 1 : 0;
+    p.causal = causal;
     if (d <= 32) return launch_simt<32>(p, st);
     if (d <= 64) return launch_simt<64>(p, st);
     if (d <= 96) return launch_simt<96>(p, st);
@@ -306,6 +314,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     int B, int H, int N, int d, float scale, int causal, void* stream) {
   t_err[0] = '\0';
   fa_status s;
+  if ((s = check_causal(causal)) != FA_OK) return s;
   if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
   if (!dO || !lse || !dq || !dk || !dv || !workspace)
     return fail(FA_ERR_INVALID, "dO, lse, dq, dk, dv and workspace must be non-null device pointers");
@@ -480,6 +489,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     float scale, int causal, void* stream) {
   t_err[0] = '\0';
   fa_status s;
+  if ((s = check_causal(causal)) != FA_OK) return s;
   if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
   if (!dO || !lse || !dq || !dk || !dv)
     return fail(FA_ERR_INVALID, "dO, lse, dq, dk and dv must be non-null device pointers");

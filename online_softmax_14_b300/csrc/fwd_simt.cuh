@@ -26,7 +26,7 @@ struct SimtParams {
   int BH, H, N, d;
   float scale;        // score multiplier (> 0)
   float scale_log2;   // scale * log2(e)
-  int causal;
+  int causal;         // 0 none, 1 key k visible iff k <= row, 2 iff k < row
 };
 
 constexpr int SIMT_ROWS = 8;   // query rows (warps) per CTA
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(SIMT_ROWS * 32) fwd_f32_simt_kernel(const Simt
 #pragma unroll 8
     for (int c = 0; c < DP; ++c) s = fmaf(sQ[warp][c], sK[lane][c], s);
     const int key = k0 + lane;
-    const bool vis = key < kv_limit && (!p.causal || key <= row);
+    const bool vis = key < kv_limit && (!p.causal || key < row + (p.causal == 2 ? 0 : 1));
     if (!vis) s = -INFINITY;
 
     float mb = s;  // block max (warp reduction)

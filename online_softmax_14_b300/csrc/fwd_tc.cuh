@@ -59,7 +59,8 @@ struct TcParams {
   int BH, H, N;
   int n_qt;           // query tiles per head
   float scale_log2;   // scale * log2(e), > 0
-  int causal;
+  int causal;         // 0 none, 1 key k visible iff k <= row, 2 iff k < row
+  int cdiag;          // 1 when the diagonal key is visible (causal 1), else 0
   unsigned* status;
   unsigned long long timeout_ns;
   int inject;         // test hook: 1 = producer stops after the first K/V tile
@@ -272,9 +273,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + (ti ? L::TM_S1 : L::TM_S0);
     const uint32_t o_col = lane_base + (ti ? L::TM_O1 : L::TM_O0);
-    const int qrow = q0 + ti * L::BM + r;
+    // row + cdiag: key k is visible to this row iff k < qlim (causal modes)
+    const int qlim = q0 + ti * L::BM + r + p.cdiag;
     const int n_kv = ti ? n_t1 : n_t0;
-    const int qt0 = q0 + ti * L::BM;  // first row of this tile
+    const int qt0c = q0 + ti * L::BM + p.cdiag;  // qlim of the tile's first row
     const float sl = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -297,9 +299,10 @@ __global__ void __launch_bounds__(384, 1)
       FA_REG_FENCE32(sr + 96);
 
       const int k0 = j * L::BN;
-      if (k0 + L::BN > kv_limit || (p.causal && k0 + L::BN - 1 > qt0)) {
+      // causal: key k visible iff k < row + cdiag (cdiag 1: k <= row; 0: strict)
+      if (k0 + L::BN > kv_limit || (p.causal && k0 + L::BN > qt0c)) {
         int lim = kv_limit - k0;
-        if (p.causal) lim = min(lim, qrow - k0 + 1);
+        if (p.causal) lim = min(lim, qlim - k0);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= lim) sr[i] = __float_as_uint(-INFINITY);
@@ -360,7 +363,8 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     if (ok && n_kv > 0 && !__all_sync(0xffffffffu, mbar_wait(&o_done[ti], 0, wc, ST_TIMEOUT_O))) ok = false;
-    if (ok && qt0 < p.N) {
+    const int qrow = qlim - p.cdiag;
+    if (ok && qt0c - p.cdiag < p.N) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;  // guard: l = 0 -> zero vector
       const size_t orow = (static_cast<size_t>(bh) * p.N + qrow) * D;

@@ -72,6 +72,8 @@ def _fwd_ex(dtype=0, q=P, k=P, v=P, o=P, lse=None, kv=None, Bs=1, H=1, N=16, d=6
     (dict(dtype=1, d=129), B.FA_ERR_UNSUPPORTED),
     (dict(dtype=1, v=P + 2), B.FA_ERR_INVALID),  # fp32 needs 4-byte alignment
     (dict(dtype=7), B.FA_ERR_INVALID),
+    (dict(causal=3), B.FA_ERR_INVALID),          # causal is 0, 1 or 2
+    (dict(causal=-1), B.FA_ERR_INVALID),
 ])
 def test_host_validation(kw, status):
     assert _fwd_ex(**kw) == status
@@ -117,6 +119,7 @@ def test_bwd_workspace_size():
     (dict(N=0), B.FA_ERR_INVALID),
     (dict(scale=float("nan")), B.FA_ERR_INVALID),
     (dict(d=64), B.FA_ERR_UNSUPPORTED),
+    (dict(causal=5), B.FA_ERR_INVALID),
 ])
 def test_bwd_host_validation(kw, status):
     assert _bwd(**kw) == status

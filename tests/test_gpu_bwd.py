@@ -131,3 +131,12 @@ def test_bwd_repeatable():
     b = run_fwd_bwd(pr, causal=True)
     for x, y in zip(a, b):
         assert np.abs(x - y).max() <= 1e-5
+
+
+@pytest.mark.parametrize("N", [64, 200, 384])
+def test_bwd_strictly_causal(N):
+    """Strictly causal gradients (Cell D2's setting): query 0 takes part in
+    nothing, so its dQ row is zero, and the last key is seen by no query."""
+    (dq, dk, dv), _ = bwd_parity(2, 2, N, 2, seed=N + 7)
+    assert np.all(dq[:, :, 0] == 0)
+    assert np.all(dk[:, :, N - 1] == 0) and np.all(dv[:, :, N - 1] == 0)

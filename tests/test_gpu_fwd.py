@@ -205,3 +205,25 @@ def test_starved_pipeline_times_out_and_recovers():
         m.fa_set_wait_timeout_ms(1000)
     m.fa_check_device_error()  # status word was cleared
     full_parity(1, 2, 512, 128, causal=False, seed=8)
+
+
+# ------------------------------------------------- strictly causal (Cell D2)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 130, 300, 513])
+def test_bf16_strictly_causal(N, d):
+    """Key j is visible to query i only when j < i (Worked examples, Cell D2's
+    strictly causal setup): query 0 sees no key, so O = 0 and lse = -inf."""
+    o, lse = full_parity(2, 2, N, d, causal=2, seed=N + d)
+    assert np.all(o[:, :, 0] == 0.0) and np.all(np.isneginf(lse[:, :, 0]))
+    if N > 1:
+        assert np.all(np.isfinite(lse[:, :, 1:]))
+
+
+def test_bf16_strictly_causal_with_padding():
+    full_parity(4, 2, 260, 128, causal=2, kv_len=[0, 1, 2, 260], seed=31)
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_fp32_strictly_causal(d):
+    o, lse = full_parity(2, 2, 77, d, causal=2, dtype="fp32", seed=d + 1)
+    assert np.all(o[:, :, 0] == 0.0) and np.all(np.isneginf(lse[:, :, 0]))
