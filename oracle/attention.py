@@ -27,7 +27,8 @@ Sources (page title, then section):
 
 Readings where the pages are silent (each is listed in the design notes):
   * causal is inclusive (j <= i) with queries and keys indexed alike; the
-    strictly causal mode (j < i) is Cell D2's setting;
+    strictly causal mode (j < i) is Cell D2's setting; with Nq != Nk the queries
+    are the last Nq positions (query i at position i + Nk - Nq);
   * key padding: keys j >= kv_len[b] are masked for every head and query of batch
     b (the pages do not mention padding; it is the same -inf mask as Cell D);
   * lse is the natural log of sum_j exp(S_ij) over visible keys, i.e. m + ln l,
@@ -86,12 +87,16 @@ def visible_mask(nq: int, nk: int, causal, kv_len: int | None) -> np.ndarray:
     """Boolean [Nq, Nk]: True where query i may attend to key j.
 
     Causal (Worked examples, Cell D): key j is visible to query i iff j <= i;
-    strictly causal (Cell D2) iff j < i.  Key padding (a reading; the pages have
-    no padding): key j is visible iff j < kv_len.
+    strictly causal (Cell D2) iff j < i.  When there are fewer (or more) queries
+    than keys, the queries are taken to be the last Nq positions of the key
+    sequence -- query i sits at position i + (Nk - Nq) -- so the last query sees
+    every key (a reading: the pages only treat Nq = Nk, where this is the rule
+    above).  Key padding (a reading; the pages have no padding): key j is
+    visible iff j < kv_len.
     """
     vis = np.ones((nq, nk), dtype=bool)
     if causal:
-        vis &= key_visible(np.arange(nk)[None, :], np.arange(nq)[:, None], causal)
+        vis &= key_visible(np.arange(nk)[None, :], np.arange(nq)[:, None] + (nk - nq), causal)
     if kv_len is not None:
         vis &= np.arange(nk)[None, :] < int(kv_len)
     return vis
@@ -149,12 +154,13 @@ def _head_fwd(q, k, v, scale, causal, kv_len):
 def attention_fwd(q, k, v, scale: float, causal: bool = False, kv_len=None):
     """Exact attention forward over every (b, h).
 
-    q, k: [B, H, N, dk]; v: [B, H, N, dv] (any float type, converted exactly to
-    float64); scale: the score multiplier (1/sqrt(dk) in the pages); causal: 0
-    (none), 1 (inclusive, j <= i) or 2 (strict, j < i); kv_len: None or B
-    integers in [0, N].
+    q: [B, H, Nq, dk]; k: [B, H, Nk, dk]; v: [B, H, Nk, dv] (Nq may differ from
+    Nk; any float type, converted exactly to float64); scale: the score
+    multiplier (1/sqrt(dk) in the pages); causal: 0 (none), 1 (inclusive,
+    j <= i + Nk - Nq) or 2 (strict, j < i + Nk - Nq); kv_len: None or B integers
+    in [0, Nk].
 
-    Returns (O [B, H, N, dv] float64, lse [B, H, N] float64).
+    Returns (O [B, H, Nq, dv] float64, lse [B, H, Nq] float64).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, _ = q.shape
@@ -177,6 +183,7 @@ def attention_fwd_rows(q, k, v, scale: float, causal: bool, kv_len, rows):
     """
     out_o, out_lse = [], []
     scale = float(scale)
+    nq = q.shape[2]
     for (b, h, i) in rows:
         qi = _f64(q[b, h, i : i + 1])
         kk = _f64(k[b, h])
@@ -185,7 +192,7 @@ def attention_fwd_rows(q, k, v, scale: float, causal: bool, kv_len, rows):
         s = score_matrix(qi, kk, scale)
         vis = np.ones((1, nk), dtype=bool)
         if causal:
-            vis &= key_visible(np.arange(nk)[None, :], i, causal)
+            vis &= key_visible(np.arange(nk)[None, :], i + (nk - nq), causal)
         if kv_len is not None:
             vis &= np.arange(nk)[None, :] < int(kv_len[b])
         s = apply_mask(s, vis)

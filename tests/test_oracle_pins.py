@@ -124,3 +124,33 @@ def test_strictly_causal_cell_d2():
     dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.5, causal=oracle.STRICT)
     assert np.all(dq[0, 0, 0] == 0)                       # query 0 took part in nothing
     assert np.all(dk[0, 0, N - 1] == 0) and np.all(dv[0, 0, N - 1] == 0)  # the last key is seen by no query
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 9), (3, 9), (9, 4), (5, 5)])
+@pytest.mark.parametrize("causal", [1, 2])
+def test_fewer_or_more_queries_than_keys(nq, nk, causal):
+    """With Nq != Nk the queries are the last Nq positions: query i sits at key
+    position i + Nk - Nq.  Each row must equal unmasked attention over exactly
+    the keys it may see (brute force by slicing); a row that sees no key gives
+    O = 0, lse = -inf.  A single query with every key visible is plain
+    attention over all keys (the decode case)."""
+    rng = np.random.default_rng(nq * 10 + nk + causal)
+    d = 3
+    q = rng.standard_normal((1, 2, nq, d))
+    k, v = (rng.standard_normal((1, 2, nk, d)) for _ in range(2))
+    o, lse = oracle.attention_fwd(q, k, v, 0.6, causal=causal)
+    assert o.shape == (1, 2, nq, d) and lse.shape == (1, 2, nq)
+    for i in range(nq):
+        last = i + nk - nq if causal == 1 else i + nk - nq - 1   # last visible key
+        if last < 0:
+            assert np.all(o[0, :, i] == 0) and np.all(np.isneginf(lse[0, :, i]))
+            continue
+        oi, li = oracle.attention_fwd(q[:, :, i:i + 1], k[:, :, :last + 1], v[:, :, :last + 1], 0.6)
+        assert np.allclose(o[:, :, i], oi[:, :, 0], rtol=1e-14) and np.allclose(lse[:, :, i], li[:, :, 0])
+    if nq == 1 and causal == 1:
+        o_all, lse_all = oracle.attention_fwd(q, k, v, 0.6)
+        assert np.allclose(o, o_all, rtol=1e-14) and np.allclose(lse, lse_all, rtol=1e-14)
+    rows = [(0, h, i) for h in range(2) for i in range(nq)]
+    o_r, l_r = oracle.attention_fwd_rows(q, k, v, 0.6, causal, None, rows)
+    assert np.allclose(o_r, o[0].reshape(-1, d), rtol=1e-14)
+    assert np.array_equal(np.isneginf(l_r), np.isneginf(lse[0].reshape(-1)))
