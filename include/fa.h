@@ -80,6 +80,21 @@ fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void
                     const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * fa_fwd_qk -- as fa_fwd_ex, with Nq queries and Nk keys per (batch, head):
+ * q, o are [B, H, Nq, d], lse is [B, H, Nq], k, v are [B, H, Nk, d].  The
+ * queries are taken to be the last Nq positions of the key sequence (query i
+ * at position i + Nk - Nq), so under causal = 1 query i sees keys
+ * j <= i + Nk - Nq and the last query sees every key; causal = 2 excludes the
+ * query's own position; a query that sees no key gets O = 0, lse = -inf.  With
+ * Nq = Nk this is exactly fa_fwd_ex.  kv_len values are clamped to [0, Nk].
+ * (The source pages treat Nq = Nk; this placement is the reading used for
+ * decoding and chunked prefill.)
+ */
+fa_status fa_fwd_qk(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* kv_len, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    void* stream);
+
+/*
  * fa_bwd_workspace_size -- bytes of device workspace fa_bwd / fa_bwd_ex need for
  * this problem: two float32 arrays of B*H*Np entries, Np = N rounded up to a
  * multiple of 64 (per-row D = rowsum(dO * O) and lse * log2(e)).  Returns 0 for

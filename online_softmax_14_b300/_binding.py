@@ -32,6 +32,8 @@ _lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_fwd.restype = _i
 _lib.fa_fwd_ex.argtypes = [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_fwd_ex.restype = _i
+_lib.fa_fwd_qk.argtypes = [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_fwd_qk.restype = _i
 _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 _lib.fa_last_error_string.argtypes = []
@@ -176,6 +178,11 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, s
                                _ptr(dv), B, H, N, d, float(scale), _causal(causal), _stream(stream)))
 
 
+def fa_fwd_qk(dtype, q, k, v, o, lse, kv_len, B, H, Nq, Nk, d, scale, causal, stream=None) -> None:
+    _check(_lib.fa_fwd_qk(int(dtype), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(kv_len), B, H, Nq, Nk, d,
+                          float(scale), _causal(causal), _stream(stream)))
+
+
 def fa_check_device_error(stream=None) -> None:
     _check(_lib.fa_check_device_error(_stream(stream)))
 
@@ -187,24 +194,28 @@ def fa_status_raw(fn_name: str, *args) -> int:
 
 
 def attention_fwd(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
-    """O, lse = attention over [B, H, N, d] CUDA tensors (bf16 or fp32, contiguous).
+    """O, lse = attention of q [B, H, Nq, d] over k, v [B, H, Nk, d] (CUDA
+    tensors, bf16 or fp32, contiguous; Nq may differ from Nk, see fa_fwd_qk).
 
     Allocates O (same dtype as q) and lse (fp32) with PyTorch, then runs
-    ``fa_fwd_ex`` on ``stream`` (default: the current stream).
+    ``fa_fwd_qk`` on ``stream`` (default: the current stream).
     """
     if q.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("q, k, v must be bfloat16 or float32")
     for t in (q, k, v):
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype and t.shape == q.shape):
-            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype and shape [B, H, N, d]")
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype and t.dim() == 4):
+            raise ValueError("q, k, v must be contiguous 4-D CUDA tensors of one dtype")
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q [B, H, Nq, d] and k, v [B, H, Nk, d] must agree in B, H and d")
     B, H, N, d = q.shape
+    Nk = k.shape[2]
     if scale is None:
         scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if kv_len is not None:
         kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
-    fa_fwd_ex(FA_BF16 if q.dtype == torch.bfloat16 else FA_FP32, q, k, v, o, lse, kv_len, B, H, N, d, scale,
+    fa_fwd_qk(FA_BF16 if q.dtype == torch.bfloat16 else FA_FP32, q, k, v, o, lse, kv_len, B, H, N, Nk, d, scale,
               causal, stream)
     return o, lse
 

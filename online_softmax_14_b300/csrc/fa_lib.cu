@@ -135,6 +135,11 @@ fa_status check_causal(int causal) {
   return FA_OK;
 }
 
+// Causal rule in the kernels' form, key j visible to query i iff j < i + qoff:
+// the queries are the last Nq positions of the key sequence (query i at
+// position i + Nk - Nq), and the strict mode excludes the query's own position.
+int causal_qoff(int Nq, int Nk, int causal) { return (Nk - Nq) + (causal == 2 ? 0 : 1); }
+
 fa_status check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
                        int N, int d, float scale, uintptr_t align) {
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID, "q, k, v and o must be non-null device pointers");
@@ -152,14 +157,14 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
 
 template <int D, int STAGES>
 fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len, int B,
-                    int H, int N, float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
+                    int H, int N, int Nk, float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
   using L = fa::TcLayout<D, STAGES>;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   fa_status s;
   if ((s = make_map(&mq, q, D, N, BH, "q")) != FA_OK) return s;
-  if ((s = make_map(&mk, k, D, N, BH, "k")) != FA_OK) return s;
-  if ((s = make_map(&mv, v, D, N, BH, "v")) != FA_OK) return s;
+  if ((s = make_map(&mk, k, D, Nk, BH, "k")) != FA_OK) return s;
+  if ((s = make_map(&mv, v, D, Nk, BH, "v")) != FA_OK) return s;
   fa::TcParams p{};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -167,10 +172,11 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
   p.BH = BH;
   p.H = H;
   p.N = N;
+  p.Nk = Nk;
   p.n_qt = (N + 127) / 128;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal = causal;
-  p.cdiag = (causal == 2) ? 0 : 1;
+  p.qoff = causal_qoff(N, Nk, causal);
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.load();
@@ -257,22 +263,25 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
 
 extern "C" {
 
-fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
-                    const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream) {
+fa_status fa_fwd_qk(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* kv_len, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    void* stream) {
   t_err[0] = '\0';
   fa_status s;
   if ((s = check_causal(causal)) != FA_OK) return s;
+  if (Nk < 1) return fail(FA_ERR_INVALID, "Nk must be >= 1 (got %d)", Nk);
+  if (static_cast<long long>(Nk) * d > (1ll << 38)) return fail(FA_ERR_UNSUPPORTED, "problem too large (Nk*d)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == FA_BF16) {
-    if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
+    if ((s = check_common(q, k, v, o, lse, B, H, Nq, d, scale, 16)) != FA_OK) return s;
     if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "bf16 path serves d = 64 or 128 (got %d)", d);
     DeviceState* ds = nullptr;
     if ((s = device_state(&ds)) != FA_OK) return s;
-    if (d == 128) return launch_tc<128, kSlotsD128>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
-    return launch_tc<64, kSlotsD64>(q, k, v, o, lse, kv_len, B, H, N, scale, causal, st, *ds);
+    if (d == 128) return launch_tc<128, kSlotsD128>(q, k, v, o, lse, kv_len, B, H, Nq, Nk, scale, causal, st, *ds);
+    return launch_tc<64, kSlotsD64>(q, k, v, o, lse, kv_len, B, H, Nq, Nk, scale, causal, st, *ds);
   }
   if (dtype == FA_FP32) {
-    if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 4)) != FA_OK) return s;
+    if ((s = check_common(q, k, v, o, lse, B, H, Nq, d, scale, 4)) != FA_OK) return s;
     if (d > 128) return fail(FA_ERR_UNSUPPORTED, "fp32 path serves d <= 128 (got %d)", d);
     if (static_cast<long long>(B) * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fp32 path serves B*H <= 65535");
     DeviceState* ds = nullptr;
@@ -286,17 +295,24 @@ fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void
     p.kv_len = kv_len;
     p.BH = B * H;
     p.H = H;
-    p.N = N;
+    p.N = Nq;
+    p.Nk = Nk;
     p.d = d;
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.causal = causal;
+    p.qoff = causal_qoff(Nq, Nk, causal);
     if (d <= 32) return launch_simt<32>(p, st);
     if (d <= 64) return launch_simt<64>(p, st);
     if (d <= 96) return launch_simt<96>(p, st);
     return launch_simt<128>(p, st);
   }
   return fail(FA_ERR_INVALID, "unknown dtype %d", dtype);
+}
+
+fa_status fa_fwd_ex(int dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* kv_len, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  return fa_fwd_qk(dtype, q, k, v, o, lse, kv_len, B, H, N, N, d, scale, causal, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,

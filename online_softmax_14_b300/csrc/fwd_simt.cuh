@@ -23,10 +23,12 @@ struct SimtParams {
   float* o;
   float* lse;         // may be null
   const int* kv_len;  // may be null
-  int BH, H, N, d;
+  int BH, H, N, d;    // N queries per head
+  int Nk;             // keys per head
   float scale;        // score multiplier (> 0)
   float scale_log2;   // scale * log2(e)
-  int causal;         // 0 none, 1 key k visible iff k <= row, 2 iff k < row
+  int causal;         // 0 none, else key k visible to row i iff k < i + qoff
+  int qoff;           // (Nk - N) + 1 (causal 1) or (Nk - N) (causal 2, strict)
 };
 
 constexpr int SIMT_ROWS = 8;   // query rows (warps) per CTA
@@ -44,14 +46,15 @@ __global__ void __launch_bounds__(SIMT_ROWS * 32) fwd_f32_simt_kernel(const Simt
   const int b = bh / p.H;
   const int row0 = blockIdx.x * SIMT_ROWS;
   const int row = row0 + warp;
-  const int N = p.N, d = p.d;
-  const size_t head = static_cast<size_t>(bh) * N * d;
+  const int N = p.N, Nk = p.Nk, d = p.d;
+  const size_t head = static_cast<size_t>(bh) * N * d;     // q, o
+  const size_t head_k = static_cast<size_t>(bh) * Nk * d;  // k, v
 
-  int kv_limit = N;
-  if (p.kv_len) kv_limit = min(N, max(0, p.kv_len[b]));
-  // keys this CTA needs: causal rows see keys <= row; padding stops at kv_limit
+  int kv_limit = Nk;
+  if (p.kv_len) kv_limit = min(Nk, max(0, p.kv_len[b]));
+  // keys this CTA needs: causal rows see keys < row + qoff; padding stops at kv_limit
   int n_keys = kv_limit;
-  if (p.causal) n_keys = min(n_keys, min(N, row0 + SIMT_ROWS));
+  if (p.causal) n_keys = min(n_keys, max(0, row0 + SIMT_ROWS - 1 + p.qoff));
 
   for (int c = lane; c < DP; c += 32)
     sQ[warp][c] = (row < N && c < d) ? p.q[head + static_cast<size_t>(row) * d + c] : 0.f;
@@ -65,8 +68,8 @@ __global__ void __launch_bounds__(SIMT_ROWS * 32) fwd_f32_simt_kernel(const Simt
     __syncthreads();
     for (int idx = threadIdx.x; idx < SIMT_KEYS * DP; idx += blockDim.x) {
       const int kr = idx / DP, c = idx % DP;
-      const bool in = (k0 + kr < N) && c < d;
-      const size_t g = head + static_cast<size_t>(k0 + kr) * d + c;
+      const bool in = (k0 + kr < Nk) && c < d;
+      const size_t g = head_k + static_cast<size_t>(k0 + kr) * d + c;
       sK[kr][c] = in ? p.k[g] : 0.f;
       sV[kr][c] = in ? p.v[g] : 0.f;
     }
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(SIMT_ROWS * 32) fwd_f32_simt_kernel(const Simt
 #pragma unroll 8
     for (int c = 0; c < DP; ++c) s = fmaf(sQ[warp][c], sK[lane][c], s);
     const int key = k0 + lane;
-    const bool vis = key < kv_limit && (!p.causal || key < row + (p.causal == 2 ? 0 : 1));
+    const bool vis = key < kv_limit && (!p.causal || key < row + p.qoff);
     if (!vis) s = -INFINITY;
 
     float mb = s;  // block max (warp reduction)

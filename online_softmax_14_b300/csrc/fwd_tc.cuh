@@ -57,10 +57,12 @@ struct TcParams {
   float* lse;         // [B, H, N] or null
   const int* kv_len;  // [B] or null
   int BH, H, N;
+  int Nk;             // keys per head (N is the number of queries)
   int n_qt;           // query tiles per head
   float scale_log2;   // scale * log2(e), > 0
   int causal;         // 0 none, 1 key k visible iff k <= row, 2 iff k < row
-  int cdiag;          // 1 when the diagonal key is visible (causal 1), else 0
+  int qoff;           // causal: key k is visible to query row i iff k < i + qoff, where
+                      // qoff = (Nk - N) + 1 (causal 1) or (Nk - N) (causal 2, strict)
   unsigned* status;
   unsigned long long timeout_ns;
   int inject;         // test hook: 1 = producer stops after the first K/V tile
@@ -114,12 +116,18 @@ __global__ void __launch_bounds__(384, 1)
   const int pr = n_pair - 1 - static_cast<int>(blockIdx.x) % n_pair;
   const int b = bh / p.H;
   const int q0 = pr * 2 * L::BM;  // first row of tile 0; tile 1 starts at q0 + 128
-  int kv_limit = p.N;
-  if (p.kv_len) kv_limit = min(p.N, max(0, p.kv_len[b]));
+  int kv_limit = p.Nk;
+  if (p.kv_len) kv_limit = min(p.Nk, max(0, p.kv_len[b]));
   const int n_kv_all = (kv_limit + L::BN - 1) / L::BN;
-  // key tiles each query tile needs (0 for a tile entirely past N)
-  const int n_t0 = p.causal ? min(n_kv_all, 2 * pr + 1) : n_kv_all;
-  const int n_t1 = (2 * pr + 1 < p.n_qt) ? (p.causal ? min(n_kv_all, 2 * pr + 2) : n_kv_all) : 0;
+  // key tiles query tile qt needs (0 for a tile entirely past N): under a causal
+  // mask, up to the tile holding the last key its last row can see
+  auto tiles = [&](int qt) -> int {
+    if (qt >= p.n_qt) return 0;
+    if (!p.causal) return n_kv_all;
+    const int last_key = min(qt * L::BM + L::BM, p.N) - 1 + p.qoff - 1;
+    return last_key < 0 ? 0 : min(n_kv_all, last_key / L::BN + 1);
+  };
+  const int n_t0 = tiles(2 * pr), n_t1 = tiles(2 * pr + 1);
   const int n_max = max(n_t0, n_t1);
 
   if (threadIdx.x == 0) {
@@ -273,10 +281,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + (ti ? L::TM_S1 : L::TM_S0);
     const uint32_t o_col = lane_base + (ti ? L::TM_O1 : L::TM_O0);
-    // row + cdiag: key k is visible to this row iff k < qlim (causal modes)
-    const int qlim = q0 + ti * L::BM + r + p.cdiag;
+    // key k is visible to this row iff k < qlim (causal modes)
+    const int qlim = q0 + ti * L::BM + r + p.qoff;
     const int n_kv = ti ? n_t1 : n_t0;
-    const int qt0c = q0 + ti * L::BM + p.cdiag;  // qlim of the tile's first row
+    const int qt0c = q0 + ti * L::BM + p.qoff;  // qlim of the tile's first row
     const float sl = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(384, 1)
       FA_REG_FENCE32(sr + 96);
 
       const int k0 = j * L::BN;
-      // causal: key k visible iff k < row + cdiag (cdiag 1: k <= row; 0: strict)
+      // causal: key k visible iff k < row + qoff
       if (k0 + L::BN > kv_limit || (p.causal && k0 + L::BN > qt0c)) {
         int lim = kv_limit - k0;
         if (p.causal) lim = min(lim, qlim - k0);
@@ -363,8 +371,8 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     if (ok && n_kv > 0 && !__all_sync(0xffffffffu, mbar_wait(&o_done[ti], 0, wc, ST_TIMEOUT_O))) ok = false;
-    const int qrow = qlim - p.cdiag;
-    if (ok && qt0c - p.cdiag < p.N) {
+    const int qrow = qlim - p.qoff;
+    if (ok && qt0c - p.qoff < p.N) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;  // guard: l = 0 -> zero vector
       const size_t orow = (static_cast<size_t>(bh) * p.N + qrow) * D;

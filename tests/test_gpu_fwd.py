@@ -227,3 +227,53 @@ def test_bf16_strictly_causal_with_padding():
 def test_fp32_strictly_causal(d):
     o, lse = full_parity(2, 2, 77, d, causal=2, dtype="fp32", seed=d + 1)
     assert np.all(o[:, :, 0] == 0.0) and np.all(np.isneginf(lse[:, :, 0]))
+
+
+# -------------------------------- queries and keys of different lengths
+def _qk_problem(B, H, Nq, Nk, d, dtype, seed, padded=False):
+    """q from one draw of length Nq, k and v from another of length Nk."""
+    pq = make_problem(B, H, Nq, d, dtype, seed=seed)
+    pk = make_problem(B, H, Nk, d, dtype, seed=seed + 1000, padded=padded)
+    return pq["q"], pk["k"], pk["v"], pq["scale"], pk["kv_len"]
+
+
+def qk_parity(B, H, Nq, Nk, d, causal, dtype="bf16", seed=0, padded=False):
+    q, k, v, scale, kl = _qk_problem(B, H, Nq, Nk, d, dtype, seed, padded)
+    o, lse = fa().attention_fwd(q.to(DEV), k.to(DEV), v.to(DEV), scale, causal=causal,
+                                kv_len=None if kl is None else kl.to(DEV))
+    fa().fa_check_device_error()
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    kll = None if kl is None else kl.tolist()
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, scale, causal=causal, kv_len=kll)
+    check(o, lse, o_ref, lse_ref, fp32=(dtype == "fp32"), label=f"Nq{Nq} Nk{Nk} d{d} c{causal} kv{kll}")
+    return o, lse
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+@pytest.mark.parametrize("Nq,Nk", [(1, 300), (64, 513), (200, 130), (129, 1000), (384, 256)])
+def test_bf16_queries_and_keys_differ(Nq, Nk, causal, d):
+    """Nq != Nk: the queries are the last Nq positions of the key sequence."""
+    qk_parity(2, 2, Nq, Nk, d, causal, seed=Nq + Nk + causal)
+
+
+def test_bf16_queries_and_keys_differ_padded():
+    qk_parity(5, 2, 100, 400, 128, 1, seed=41, padded=True)
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_fp32_queries_and_keys_differ(causal):
+    qk_parity(2, 2, 37, 101, 64, causal, dtype="fp32", seed=42 + causal)
+    qk_parity(2, 2, 101, 37, 64, causal, dtype="fp32", seed=45 + causal)
+
+
+def test_decode_single_query_sees_every_key():
+    """One query per head under the causal mask is the last position: it attends
+    to every key, i.e. equals attention with no mask."""
+    q, k, v, scale, _ = _qk_problem(3, 4, 1, 777, 128, "bf16", seed=50)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o_c, l_c = fa().attention_fwd(qd, kd, vd, scale, causal=True)
+    o_n, l_n = fa().attention_fwd(qd, kd, vd, scale, causal=False)
+    fa().fa_check_device_error()
+    assert torch.equal(o_c, o_n) and torch.equal(l_c, l_n)
