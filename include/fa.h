@@ -97,7 +97,7 @@ fa_status fa_fwd_qk(int dtype, const void* q, const void* k, const void* v, void
 /*
  * fa_bwd_workspace_size -- bytes of device workspace fa_bwd / fa_bwd_ex need for
  * this problem: two float32 arrays of B*H*Np entries, Np = N rounded up to a
- * multiple of 64 (per-row D = rowsum(dO * O) and lse * log2(e)).  Returns 0 for
+ * multiple of 128 (per-row D = rowsum(dO * O) and lse * log2(e)).  Returns 0 for
  * non-positive sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -169,7 +169,7 @@ fa_status fa_merge(int dtype, const void* o_parts, const float* lse_parts, int n
  *   dq, dk, dv are still the caller's device memory.  The library allocates
  *   nothing, through the CUDA runtime or otherwise.
  *   Limit: B * H * Np <= FA_BWD_NOALLOC_MAX_ROWS, where Np is N rounded up to
- *   a multiple of 64.  Larger problems return FA_ERR_UNSUPPORTED with a message
+ *   a multiple of 128.  Larger problems return FA_ERR_UNSUPPORTED with a message
  *   naming the limit; use fa_bwd with a workspace for them.
  *   The first call on each device looks up the array's device address with
  *   cudaGetSymbolAddress, so make that first call before any stream capture.

@@ -12,7 +12,7 @@
 //
 // Two kernels:
 //  * bwd_preprocess_kernel -- D_i and lse2_i = lse_i log2(e) into the workspace
-//    (row stride Np = N rounded up to 64; padding rows get D = 0, lse2 = +inf so
+//    (row stride Np = N rounded up to 128; padding rows get D = 0, lse2 = +inf so
 //    that their probabilities are exactly 0), and zeroes dQ.
 //  * bwd_bf16_tc_kernel -- one CTA per (batch, head, 128-key tile).  K and V stay
 //    in shared memory; the CTA streams 64-query tiles (Q_t, dO_t, lse2_t, D_t)
@@ -67,6 +67,8 @@ enum : unsigned {
   ST_BWD_TIMEOUT_DQE = 1u << 15,
   ST_BWD_TIMEOUT_EMPTY = 1u << 16,
   ST_BWD_TIMEOUT_DONE = 1u << 17,
+  ST_BWD_TIMEOUT_RED = 1u << 18,
+  ST_BWD_SMEM_ALIGN = 1u << 19,   // dynamic shared memory base not aligned enough (kernel did nothing)
 };
 
 struct BwdPreParams {
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
 }
 
 struct BwdParams {
-  float* dq;                // [BH, N, D], accumulated with red.add
+  float* dq;                // [BH, N, D], accumulated by tiled reduce-adds (tensor map tm_dq)
   float* dk;                // [BH, N, D]
   float* dv;                // [BH, N, D]
   const float* lse2;        // [BH, Np]
@@ -150,54 +152,64 @@ template <int STAGES>
 struct BwdLayout {
   static constexpr int D = 128;
   static constexpr int BN = 128;                   // keys per CTA
-  static constexpr int BM = 64;                    // queries per tile
+  static constexpr int BM = 128;                   // queries per tile
   static constexpr int KB = D / 64;                // 128-byte column blocks
-  static constexpr int KV_COLBLK = BN * 128;       // 16 KB
-  static constexpr int KV_TILE = BN * D * 2;       // 32 KB
-  static constexpr int Q_COLBLK = BM * 128;        // 8 KB
-  static constexpr int Q_TILE = BM * D * 2;        // 16 KB
-  static constexpr int DS_TILE = BN * BM * 2;      // 16 KB: 128 key rows x 128 bytes
+  static constexpr int COLBLK = 128 * 128;         // 16 KB: 128 rows x 128 bytes
+  static constexpr int TILE = 128 * D * 2;         // 32 KB: a K, V, Q or dO tile
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = KV_TILE;
-  static constexpr int OFF_Q = 2 * KV_TILE;
-  static constexpr int OFF_DO = OFF_Q + STAGES * Q_TILE;
-  static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
-  static constexpr int OFF_LSE = OFF_DS + 2 * DS_TILE;
-  static constexpr int OFF_DD = OFF_LSE + STAGES * BM * 4;
-  static constexpr int OFF_BAR = OFF_DD + STAGES * BM * 4;
-  // barriers: kv_full, q_full[S], q_empty[S], s_full[2], p_full[2], dp_full[2],
-  //           ds_full[2], dq_full[2], dq_empty, dkv_done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 * 5 + 3;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;
+  static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
+  static constexpr int OFF_DS = OFF_DO + STAGES * TILE;  // dS^T: 2 column blocks of 64 queries
+  static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: lse2[128], D[128]
+  static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
+  // barriers: kv_full, q_full[S], q_empty[S], stage_done[S], s_full, p_full, dp_full, ds_full,
+  //           dq_full, dq_empty, red_ready[2], dkv_done, drain
+  static constexpr int NBAR = 1 + 3 * STAGES + 6 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int USED = OFF_MISC + 16;
+  static constexpr int BYTES = 232448;             // the whole per-CTA budget
+  static constexpr int SLACK = BYTES - USED;        // room to align the base up to 1024 bytes
+  // S^T, then P^T (bf16, in each half's own columns), | dP^T, then dQ^T | dV | dK
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
-  static constexpr uint32_t Q_TX = 2 * Q_TILE + 2 * BM * 4;
-  static_assert(BYTES <= 232448, "shared memory budget");
+  static_assert(SLACK >= 0, "shared memory budget");
 };
 
 template <int STAGES>
 __global__ void __launch_bounds__(384, 1)
     bwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using L = BwdLayout<STAGES>;
   constexpr int D = L::D;
   extern __shared__ uint8_t smem_raw[];
+  {
+    // the layout fills the budget but for SLACK bytes: the base must be aligned
+    // to within SLACK of 1024 bytes (it is 1024-aligned in practice)
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad > static_cast<uint32_t>(L::SLACK)) {
+      if (threadIdx.x == 0) atomicOr(p.status, ST_BWD_SMEM_ALIGN);
+      return;
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* q_full = kv_full + 1;
   uint64_t* q_empty = q_full + STAGES;
-  uint64_t* s_full = q_empty + STAGES;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* dp_full = p_full + 2;
-  uint64_t* ds_full = dp_full + 2;
-  uint64_t* dq_full = ds_full + 2;
-  uint64_t* dq_empty = dq_full + 2;
-  uint64_t* dkv_done = dq_empty + 1;
+  uint64_t* stage_done = q_empty + STAGES;
+  uint64_t* s_full = stage_done + STAGES;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dp_full = p_full + 1;
+  uint64_t* ds_full = dp_full + 1;
+  uint64_t* dq_full = ds_full + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* red_ready = dq_empty + 1;  // [2]
+  uint64_t* dkv_done = red_ready + 2;
   uint64_t* drain = dkv_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  volatile int* issued = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // head-major; within a head the key tiles with the most query tiles first
@@ -215,19 +227,21 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
+      mbar_init(&q_empty[s], 2);  // both warpgroups' dQ reductions have read the stage
+      mbar_init(&stage_done[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
-      mbar_init(&dp_full[s], 1);
-      mbar_init(&ds_full[s], 128);
-      mbar_init(&dq_full[s], 1);
-    }
-    mbar_init(dq_empty, 128);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 256);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 256);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 256);
+    mbar_init(&red_ready[0], 128);
+    mbar_init(&red_ready[1], 128);
     mbar_init(dkv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *issued = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -235,6 +249,7 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::TM_COLS);
@@ -247,30 +262,30 @@ __global__ void __launch_bounds__(384, 1)
   const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
   constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
 
-  int issued = 0;  // query tiles whose loads the producer has issued
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0 && n_it > 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * L::KV_TILE);
+      mbar_arrive_expect_tx(kv_full, 2 * L::TILE);
 #pragma unroll
       for (int kb = 0; kb < L::KB; ++kb) {
-        tma_load_3d(smem + L::OFF_K + kb * L::KV_COLBLK, &tm_k, kv_full, kb * 64, k0, bh);
-        tma_load_3d(smem + L::OFF_V + kb * L::KV_COLBLK, &tm_v, kv_full, kb * 64, k0, bh);
+        tma_load_3d(smem + L::OFF_K + kb * L::COLBLK, &tm_k, kv_full, kb * 64, k0, bh);
+        tma_load_3d(smem + L::OFF_V + kb * L::COLBLK, &tm_v, kv_full, kb * 64, k0, bh);
       }
       for (int t = 0; t < n_it; ++t) {
         const int st = t % STAGES;
         if (t >= STAGES && !mbar_wait(&q_empty[st], ((t / STAGES) - 1) & 1, wc, ST_BWD_TIMEOUT_EMPTY)) break;
         const int q0 = (i0 + t) * L::BM;
-        mbar_arrive_expect_tx(&q_full[st], L::Q_TX);
+        mbar_arrive_expect_tx(&q_full[st], 2 * L::TILE + 1024);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb) {
-          tma_load_3d(smem + L::OFF_Q + st * L::Q_TILE + kb * L::Q_COLBLK, &tm_q, &q_full[st], kb * 64, q0, bh);
-          tma_load_3d(smem + L::OFF_DO + st * L::Q_TILE + kb * L::Q_COLBLK, &tm_do, &q_full[st], kb * 64, q0, bh);
+          tma_load_3d(smem + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, &q_full[st], kb * 64, q0, bh);
+          tma_load_3d(smem + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, &q_full[st], kb * 64, q0, bh);
         }
+        // lse2 and D of the tile's 128 queries (rows padded to a multiple of 128)
         const size_t ws = static_cast<size_t>(bh) * p.Np + q0;
-        bulk_load(smem + L::OFF_LSE + st * L::BM * 4, p.lse2 + ws, L::BM * 4, &q_full[st]);
-        bulk_load(smem + L::OFF_DD + st * L::BM * 4, p.dd + ws, L::BM * 4, &q_full[st]);
-        issued = t + 1;
+        bulk_load(smem + L::OFF_STAT + st * 1024, p.lse2 + ws, 512, &q_full[st]);
+        bulk_load(smem + L::OFF_STAT + st * 1024 + 512, p.dd + ws, 512, &q_full[st]);
+        *issued = t + 1;
       }
     }
   } else if (warp == 1) {
@@ -283,76 +298,60 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
       const uint32_t sds = smem_u32(smem + L::OFF_DS);
 
-      // S^T_t (or dP^T_t): A = K (or V) K-major, B = Q_t (or dO_t) K-major
+      // S^T = K Q_t^T or dP^T = V dO_t^T: both operands K-major, two column blocks each
       auto mma_scores = [&](uint32_t d_tm, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t adesc = sdesc_sw128(a_base + (kk >> 2) * L::KV_COLBLK + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(b_base + (kk >> 2) * L::Q_COLBLK + (kk & 3) * 32, 16, 1024);
-          umma_ss(d_tm, adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
+          umma_ss(d_tm, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), IDESC_S,
+                  kk > 0 ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(kv_full, 0, wc, ST_BWD_TIMEOUT_KV);
-      if (ok) ok = mbar_wait(&q_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
-      if (ok) {
-        tc_fence_after();
-        mma_scores(tmem + L::TM_S, sk, sq);
-        umma_commit(&s_full[0]);
-        mma_scores(tmem + L::TM_DP, sv, sdo);
-        umma_commit(&dp_full[0]);
-      }
-      // Issue order per tile t: MMA3_t, then S and dP of tile t+1, then MMA4_t and
-      // MMA5_t.  The elementwise warps build P_t and dS_t while the tensor cores
-      // work on the queued products, so the pipe never waits on one tile's
-      // softmax before it can start the next tile's scores.
       for (int t = 0; ok && t < n_it; ++t) {
-        const int st = t % STAGES, pb = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        const int t1 = t + 1, st1 = t1 % STAGES;
-        // MMA3: dV += P^T_t dO_t   (A = P^T bf16 in TMEM, B = dO_t MN-major)
-        if (!mbar_wait(&p_full[pb], ph, wc, ST_BWD_TIMEOUT_P)) break;
+        const int st = t % STAGES;
+        const uint32_t ph = t & 1;
+        const uint32_t q_t = sq + st * L::TILE, do_t = sdo + st * L::TILE;
+        // MMA1: S^T_t.  The S columns are free: P_{t-1} was read by MMA3_{t-1},
+        // issued earlier (the tensor cores run in issue order).
+        if (!mbar_wait(&q_full[st], (t / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q)) break;
         tc_fence_after();
-        {
-          const uint32_t pt = tmem + L::TM_S + pb * 64;
-#pragma unroll
-          for (int kk = 0; kk < L::BM / 16; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(sdo + st * L::Q_TILE + kk * 2048, L::Q_COLBLK, 1024);
-            umma_ts(tmem + L::TM_DV, pt + kk * 8, bdesc, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        // S^T_{t+1} and dP^T_{t+1}.  Buffer (t+1)&1 last held dQ^T_{t-1}, which
-        // its warpgroup must have read out; dP buffer (t+1)&1 held dP^T_{t-1},
-        // read before dS_{t-1} was published (waited for at tile t-1).
-        if (t1 < n_it) {
-          if (!mbar_wait(&q_full[st1], (t1 / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q)) break;
-          if (t >= 1 && !mbar_wait(dq_empty, (t - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) break;
-          tc_fence_after();
-          mma_scores(tmem + L::TM_S + (t1 & 1) * 64, sk, sq + st1 * L::Q_TILE);
-          umma_commit(&s_full[t1 & 1]);
-          mma_scores(tmem + L::TM_DP + (t1 & 1) * 64, sv, sdo + st1 * L::Q_TILE);
-          umma_commit(&dp_full[t1 & 1]);
-        }
-        // MMA4: dK += dS^T_t Q_t   (A = dS^T K-major in SMEM, B = Q_t MN-major)
-        if (!mbar_wait(&ds_full[pb], ph, wc, ST_BWD_TIMEOUT_DS)) break;
+        mma_scores(tmem + L::TM_S, sk, q_t);
+        umma_commit(s_full);
+        // MMA2: dP^T_t, into the columns dQ^T_{t-1} occupied until drained
+        if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) break;
         tc_fence_after();
-        const uint32_t ds_base = sds + pb * L::DS_TILE;
+        mma_scores(tmem + L::TM_DP, sv, do_t);
+        umma_commit(dp_full);
+        // MMA3: dV += P^T_t dO_t.  A = P^T from tensor memory: queries 0-63 in
+        // columns [0, 32), queries 64-127 in [64, 96) (each half in its own
+        // S columns); B = dO_t MN-major (16 queries = 2 KB per step).
+        if (!mbar_wait(p_full, ph, wc, ST_BWD_TIMEOUT_P)) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < L::BM / 16; ++kk) {
-          const uint64_t adesc = sdesc_sw128(ds_base + kk * 32, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(sq + st * L::Q_TILE + kk * 2048, L::Q_COLBLK, 1024);
-          umma_ss(tmem + L::TM_DK, adesc, bdesc, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_ts(tmem + L::TM_DV, tmem + L::TM_S + pcol, sdesc_sw128(do_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
+                  (t > 0 || kk > 0) ? 1u : 0u);
         }
-        // MMA5: dQ^T_t = K^T dS_t into S buffer pb (P_t there was consumed by
-        // MMA3_t, which the tensor cores finish first: they run in issue order).
-        // A = K MN-major, B = dS^T read as [query][key] MN-major.
+        // MMA5: dQ^T_t = K^T dS_t into the dP columns (dP_t was read before dS_t
+        // was published).  A = K MN-major, B = dS^T read as [query][key] MN-major
+        // (two 64-query blocks, 16 KB apart).
+        if (!mbar_wait(ds_full, ph, wc, ST_BWD_TIMEOUT_DS)) break;
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < L::BN / 16; ++kk) {
-          const uint64_t adesc = sdesc_sw128(sk + kk * 2048, L::KV_COLBLK, 1024);
-          const uint64_t bdesc = sdesc_sw128(ds_base + kk * 2048, L::DS_TILE, 1024);
-          umma_ss(tmem + L::TM_S + pb * 64, adesc, bdesc, IDESC_Q, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < L::BN / 16; ++kk)
+          umma_ss(tmem + L::TM_DP, sdesc_sw128(sk + kk * 2048, L::COLBLK, 1024),
+                  sdesc_sw128(sds + kk * 2048, L::COLBLK, 1024), IDESC_Q, kk > 0 ? 1u : 0u);
+        umma_commit(dq_full);
+        // MMA4: dK += dS^T_t Q_t.  A = dS^T K-major (two 64-query blocks), B = Q_t MN-major.
+#pragma unroll
+        for (int kk = 0; kk < L::BM / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
+          umma_ss(tmem + L::TM_DK, sdesc_sw128(sds + off, 16, 1024), sdesc_sw128(q_t + kk * 2048, L::COLBLK, 1024),
+                  IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&dq_full[pb]);
-        umma_commit(&q_empty[st]);
+        umma_commit(&stage_done[st]);  // Q_t and dO_t are no longer read by the tensor cores
       }
       umma_commit(dkv_done);
       // nothing may be in flight on the tensor cores when the CTA frees TMEM
@@ -361,40 +360,50 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------- elementwise WGs --
-    const int wg = (warp - 4) >> 2;
-    const int r = (warp & 3) * 32 + lane;  // TMEM lane
+    // Both warpgroups take every tile: warpgroup h owns query columns
+    // [64 h, 64 h + 64).  Thread r is key row r (TMEM lane r) of S^T and dP^T,
+    // and head-dim column r (TMEM lane r) of dQ^T.
+    const int h = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = lane_base + L::TM_S + h * 64;   // this half's S^T, then its P^T
+    const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T, then dQ^T
     const bool key_ok = (k0 + r) < kv_limit;
     const float sl = p.scale_log2, scale = p.scale;
-    const uint32_t ds_row = smem_u32(smem + L::OFF_DS) + r * 128;
+    const uint32_t ds_row = smem_u32(smem + L::OFF_DS) + h * L::COLBLK + r * 128;
+    const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + st * 1024: lse2; + 512: D
+    // dQ staging: warpgroup 0 reuses the stage's Q buffer, warpgroup 1 its dO buffer
+    uint8_t* const stage_out = smem + (h == 0 ? L::OFF_Q : L::OFF_DO);
+    const bool leader = (r == 0);  // issues this warpgroup's dQ reduce-adds
+    int pending = -1;              // stage whose reduce-add the leader has not yet released
     bool ok = true;
-    for (int t = wg; t < n_it; t += 2) {
-      const int st = t % STAGES, pb = t & 1;
-      const uint32_t ph = (t >> 1) & 1;
-      const int q0 = (i0 + t) * L::BM;
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_full[st], (t / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q) &&
-                                       mbar_wait(&s_full[pb], ph, wc, ST_BWD_TIMEOUT_S))) {
+    for (int t = 0; t < n_it; ++t) {
+      const int st = t % STAGES;
+      const uint32_t ph = t & 1, sph = (t / STAGES) & 1;
+      const int q0 = (i0 + t) * L::BM + h * 64;  // first query of this half
+      // q_full is already complete here (S^T_t exists); waiting on it makes the
+      // stage's lse2 / D rows visible to these threads
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, ph, wc, ST_BWD_TIMEOUT_S) &&
+                                       mbar_wait(&q_full[st], sph, wc, ST_BWD_TIMEOUT_Q))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[64];
-      const uint32_t s_col = lane_base + L::TM_S + pb * 64;
       FA_TMEM_LD32(s_col + 0, sr + 0);
       FA_TMEM_LD32(s_col + 32, sr + 32);
       tmem_wait_ld();
       FA_REG_FENCE32(sr + 0);
       FA_REG_FENCE32(sr + 32);
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::OFF_LSE + st * L::BM * 4);
-      const float* dd = reinterpret_cast<const float*>(smem + L::OFF_DD + st * L::BM * 4);
-      // causal: key k0 + r is visible to query q0 + j iff j >= r - (q0 - k0), one
-      // later in the strict mode (a query does not see its own key)
+      // causal: key k0 + r is visible to query q0 + j iff j >= r - (q0 - k0),
+      // one later in the strict mode (a query does not see its own key)
       const int jmin = p.causal ? r - (q0 - k0) + (p.causal == 2 ? 1 : 0) : -1;
+      const uint32_t lse2_s = stat + st * 1024, dd_s = lse2_s + 512;
       float pr[64];
 #pragma unroll
       for (int j4 = 0; j4 < 64; j4 += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + j4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        float lv[4];
+        ld_shared_v4f(lse2_s + j4 * 4, lv);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j = j4 + u;
@@ -408,58 +417,87 @@ __global__ void __launch_bounds__(384, 1)
       FA_TMEM_ST32(s_col, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[pb]);
+      mbar_arrive(p_full);
+      // the previous tile's reduce-add has had the P phase to read its source
+      if (leader && pending >= 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&q_empty[pending]);
+        pending = -1;
+      }
 
-      if (!__all_sync(0xffffffffu, mbar_wait(&dp_full[pb], ph, wc, ST_BWD_TIMEOUT_DP))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, ph, wc, ST_BWD_TIMEOUT_DP))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t dpr[64];
-      FA_TMEM_LD32(lane_base + L::TM_DP + pb * 64 + 0, dpr + 0);
-      FA_TMEM_LD32(lane_base + L::TM_DP + pb * 64 + 32, dpr + 32);
+      FA_TMEM_LD32(dp_col + 0, dpr + 0);
+      FA_TMEM_LD32(dp_col + 32, dpr + 32);
       tmem_wait_ld();
       FA_REG_FENCE32(dpr + 0);
       FA_REG_FENCE32(dpr + 32);
       uint32_t dsk[32];
 #pragma unroll
       for (int j4 = 0; j4 < 64; j4 += 4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(dd + j4);
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+        float dv4[4];
+        ld_shared_v4f(dd_s + j4 * 4, dv4);
         float g[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) g[u] = pr[j4 + u] * (__uint_as_float(dpr[j4 + u]) - dv4[u]) * scale;
         dsk[j4 / 2] = pack_bf16x2(g[0], g[1]);
         dsk[j4 / 2 + 1] = pack_bf16x2(g[2], g[3]);
       }
-      // row r of the 128B-swizzled K-major tile: 16-byte chunk c lands at c ^ (r & 7)
-      const uint32_t row_addr = ds_row + pb * L::DS_TILE;
+      // Row r of this half's 128B-swizzled block: 16-byte chunk c lands at c ^ (r & 7).
+      // The block is free: MMA4/MMA5 of the previous tile finished before s_full
+      // (issued after them) completed.
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        st_shared_v4(row_addr + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
+        st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(&ds_full[pb]);
+      mbar_arrive(ds_full);
 
-      // dQ^T_t: lane r holds head-dim column r of query rows q0 .. q0+63
-      if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[pb], ph, wc, ST_BWD_TIMEOUT_DQ))) {
+      // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, ph, wc, ST_BWD_TIMEOUT_DQ))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t qr[64];
-      FA_TMEM_LD32(s_col + 0, qr + 0);
-      FA_TMEM_LD32(s_col + 32, qr + 32);
+      FA_TMEM_LD32(dp_col + 0, qr + 0);
+      FA_TMEM_LD32(dp_col + 32, qr + 32);
       tmem_wait_ld();
       FA_REG_FENCE32(qr + 0);
       FA_REG_FENCE32(qr + 32);
       tc_fence_before();
       mbar_arrive(dq_empty);
-      float* dst = p.dq + (static_cast<size_t>(bh) * p.N + q0) * D + r;
-      const int jn = min(64, p.N - q0);
+      // Stage the 64 x d block row-major in the stage's Q (dO) buffer, free once
+      // MMA4_t has run, and add it into global dQ with one tiled reduce-add;
+      // rows past N are skipped by the tensor map.  A warp's 32 lanes write 128
+      // consecutive bytes per store.
+      if (!__all_sync(0xffffffffu, mbar_wait(&stage_done[st], sph, wc, ST_BWD_TIMEOUT_EMPTY))) {
+        ok = false;
+        break;
+      }
+      const uint32_t out_row = smem_u32(stage_out + st * L::TILE) + r * 4;
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (j < jn) red_add_f32(dst + static_cast<size_t>(j) * D, __uint_as_float(qr[j]));
+      for (int j = 0; j < 64; ++j) st_shared_f32(out_row + j * 512, __uint_as_float(qr[j]));
+      fence_proxy_async_smem();
+      mbar_arrive(&red_ready[h]);
+      if (!__all_sync(0xffffffffu, !leader || mbar_wait(&red_ready[h], ph, wc, ST_BWD_TIMEOUT_RED))) {
+        ok = false;
+        break;
+      }
+      if (leader) {
+        tma_reduce_add_3d(&tm_dq, stage_out + st * L::TILE, 0, q0, bh);
+        bulk_commit_group();
+        pending = st;
+      }
+    }
+    if (leader) {
+      // the CTA may not exit while a reduce-add still reads its shared memory
+      bulk_wait_all();
+      if (pending >= 0) mbar_arrive(&q_empty[pending]);
     }
 
     // ------------------------------------------------------------ epilogue --
@@ -468,8 +506,8 @@ __global__ void __launch_bounds__(384, 1)
     if (ok) {
       tc_fence_after();
       const int key = k0 + r;
-      float* out = (wg == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.N + key) * D;
-      const uint32_t col = lane_base + (wg == 0 ? L::TM_DV : L::TM_DK);
+      float* out = (h == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.N + key) * D;
+      const uint32_t col = lane_base + (h == 0 ? L::TM_DV : L::TM_DK);
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t v[32];
@@ -497,7 +535,8 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 && lane == 0 && n_it > 0 && *abort_flag) {
     // an aborted CTA may not exit while copies it issued are still landing
     bool ok = mbar_wait_drain(kv_full, 0, DRAIN_NS);
-    for (int t = max(0, issued - STAGES); t < issued; ++t)
+    const int n_iss = *issued;
+    for (int t = max(0, n_iss - STAGES); t < n_iss; ++t)
       ok &= mbar_wait_drain(&q_full[t % STAGES], (t / STAGES) & 1, DRAIN_NS);
     if (!ok) atomicOr(p.status, ST_DRAIN);
   }

@@ -32,7 +32,7 @@ constexpr int kVersion = 200;  // 0.2.0
 constexpr int kMaxDevices = 64;
 constexpr int kSlotsD128 = 4;  // K/V ring slots of the forward (32 KB each at d = 128)
 constexpr int kSlotsD64 = 8;   // (16 KB each at d = 64)
-constexpr int kStagesBwd = 3;
+constexpr int kStagesBwd = 2;
 
 thread_local char t_err[512] = "";
 std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};
@@ -127,6 +127,22 @@ fa_status make_map(CUtensorMap* m, const void* base, int d, int N, int BH, const
   return FA_OK;
 }
 
+// [BH, N, d] f32 viewed as a 3-D tensor (d innermost); d x rows x 1 boxes, no
+// swizzle (a box is `rows` consecutive rows of d floats).  Used as the target of
+// tiled reduce-adds, which skip the rows past N.
+fa_status make_map_f32(CUtensorMap* m, void* base, int d, int N, int BH, const char* name, int rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return FA_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // causal: 0 none, 1 key j visible to query i iff j <= i, 2 iff j < i (strict)
@@ -197,8 +213,8 @@ fa_status launch_simt(const fa::SimtParams& p, cudaStream_t stream) {
   return FA_OK;
 }
 
-// Row stride of the backward workspace arrays: N rounded up to the 64-query tile.
-long long bwd_np(int N) { return (static_cast<long long>(N) + 63) / 64 * 64; }
+// Row stride of the backward workspace arrays: N rounded up to the 128-query tile.
+long long bwd_np(int N) { return (static_cast<long long>(N) + 127) / 128 * 128; }
 
 size_t bwd_ws_bytes(int B, int H, int N) {
   return static_cast<size_t>(2) * static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(bwd_np(N)) *
@@ -231,12 +247,13 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch bwd_preprocess_kernel");
 
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   fa_status s;
-  if ((s = make_map(&mq, q, D, N, BH, "q", 64)) != FA_OK) return s;
+  if ((s = make_map(&mq, q, D, N, BH, "q", 128)) != FA_OK) return s;
   if ((s = make_map(&mk, k, D, N, BH, "k", 128)) != FA_OK) return s;
   if ((s = make_map(&mv, v, D, N, BH, "v", 128)) != FA_OK) return s;
-  if ((s = make_map(&mdo, dO, D, N, BH, "dO", 64)) != FA_OK) return s;
+  if ((s = make_map(&mdo, dO, D, N, BH, "dO", 128)) != FA_OK) return s;
+  if ((s = make_map_f32(&mdq, dq, D, N, BH, "dq", 64)) != FA_OK) return s;
   fa::BwdParams p{};
   p.dq = dq;
   p.dk = dk;
@@ -254,7 +271,7 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.causal = causal;
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
-  fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, p);
+  fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_bf16_tc_kernel");
   return FA_OK;
 }
@@ -466,7 +483,7 @@ int fa_version(void) { return kVersion; }
 // the library holds this array until the process exits.
 //
 // Limit: the workspace is two float32 arrays of B*H*Np rows (Np = N rounded up
-// to 64), so B*H*Np may be at most FA_BWD_NOALLOC_MAX_ROWS (4 MiB in total).
+// to 128), so B*H*Np may be at most FA_BWD_NOALLOC_MAX_ROWS (4 MiB in total).
 // Calls share the array: two calls that run at the same time on the GPU (for
 // instance on different streams) overwrite each other's workspace and give
 // wrong gradients, so such calls must be ordered. Nothing in the array needs to
@@ -515,7 +532,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   const long long rows = static_cast<long long>(B) * H * bwd_np(N);
   if (rows > FA_BWD_NOALLOC_MAX_ROWS)
     return fail(FA_ERR_UNSUPPORTED,
-                "fa_bwd_noalloc: B*H*Np = %lld rows (Np = N rounded up to 64) exceeds its fixed scratch of %d rows; "
+                "fa_bwd_noalloc: B*H*Np = %lld rows (Np = N rounded up to 128) exceeds its fixed scratch of %d rows; "
                 "use fa_bwd with a caller-supplied workspace",
                 rows, (int)FA_BWD_NOALLOC_MAX_ROWS);
   DeviceState* ds = nullptr;

@@ -102,9 +102,10 @@ def _bwd(q=P, k=P, v=P, o=P, do=P, lse=P, kv=None, dq=P, dk=P, dv=P, ws=P, ws_by
 
 
 def test_bwd_workspace_size():
-    # two float32 arrays of B*H*Np, Np = N rounded up to 64
+    # two float32 arrays of B*H*Np, Np = N rounded up to 128 (the query tile)
     assert fa.fa_bwd_workspace_size(2, 3, 100, 128) == 2 * 2 * 3 * 128 * 4
-    assert fa.fa_bwd_workspace_size(1, 1, 64, 128) == 2 * 64 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 64, 128) == 2 * 128 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 129, 128) == 2 * 256 * 4
     assert fa.fa_bwd_workspace_size(0, 1, 64, 128) == 0
 
 
