@@ -163,9 +163,9 @@ struct BwdLayout {
   static constexpr int OFF_DS = OFF_DO + STAGES * TILE;  // dS^T: 2 column blocks of 64 queries
   static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: lse2[128], D[128]
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
-  // barriers: kv_full, q_full[S], q_empty[S], stage_done[S], s_full, p_full, dp_full, ds_full,
-  //           dq_full, dq_empty, red_ready[2], dkv_done, drain
-  static constexpr int NBAR = 1 + 3 * STAGES + 6 + 2 + 2;
+  // barriers: kv_full, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full, dp_full,
+  //           ds_full, dq_full, dq_empty, red_ready[2], ds_free, dkv_done, drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 2 + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int BYTES = 232448;             // the whole per-CTA budget
@@ -195,21 +195,24 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = kv_full + 1;
-  uint64_t* q_empty = q_full + STAGES;
-  uint64_t* stage_done = q_empty + STAGES;
-  uint64_t* s_full = stage_done + STAGES;
+  uint64_t* q_full = kv_full + 1;         // [S] Q_t and its lse2 / D rows have landed
+  uint64_t* do_full = q_full + STAGES;    // [S] dO_t has landed
+  uint64_t* q_empty = do_full + STAGES;   // [S] MMA4_t, the last reader of Q_t, is done
+  uint64_t* do_empty = q_empty + STAGES;  // [S] the dQ_t half staged in dO_t's buffer has been read
+  uint64_t* s_full = do_empty + STAGES;
   uint64_t* p_full = s_full + 1;
   uint64_t* dp_full = p_full + 1;
   uint64_t* ds_full = dp_full + 1;
   uint64_t* dq_full = ds_full + 1;
   uint64_t* dq_empty = dq_full + 1;
-  uint64_t* red_ready = dq_empty + 1;  // [2]
-  uint64_t* dkv_done = red_ready + 2;
+  uint64_t* red_ready = dq_empty + 1;  // [2] warpgroup h has staged its dQ_t half
+  uint64_t* ds_free = red_ready + 2;     // the dQ_t half staged in the dS buffer has been read
+  uint64_t* dkv_done = ds_free + 1;
   uint64_t* drain = dkv_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-  volatile int* issued = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+  volatile int* issued_q = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+  volatile int* issued_do = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // head-major; within a head the key tiles with the most query tiles first
@@ -227,8 +230,9 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 2);  // both warpgroups' dQ reductions have read the stage
-      mbar_init(&stage_done[s], 1);
+      mbar_init(&do_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&do_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(p_full, 256);
@@ -238,10 +242,12 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(dq_empty, 256);
     mbar_init(&red_ready[0], 128);
     mbar_init(&red_ready[1], 128);
+    mbar_init(ds_free, 1);
     mbar_init(dkv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
-    *issued = 0;
+    *issued_q = 0;
+    *issued_do = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -273,19 +279,24 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int t = 0; t < n_it; ++t) {
         const int st = t % STAGES;
-        if (t >= STAGES && !mbar_wait(&q_empty[st], ((t / STAGES) - 1) & 1, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        const uint32_t eph = ((t / STAGES) - 1) & 1;
         const int q0 = (i0 + t) * L::BM;
-        mbar_arrive_expect_tx(&q_full[st], 2 * L::TILE + 1024);
+        if (t >= STAGES && !mbar_wait(&q_empty[st], eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(&q_full[st], L::TILE + 1024);
 #pragma unroll
-        for (int kb = 0; kb < L::KB; ++kb) {
+        for (int kb = 0; kb < L::KB; ++kb)
           tma_load_3d(smem + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, &q_full[st], kb * 64, q0, bh);
-          tma_load_3d(smem + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, &q_full[st], kb * 64, q0, bh);
-        }
         // lse2 and D of the tile's 128 queries (rows padded to a multiple of 128)
         const size_t ws = static_cast<size_t>(bh) * p.Np + q0;
         bulk_load(smem + L::OFF_STAT + st * 1024, p.lse2 + ws, 512, &q_full[st]);
         bulk_load(smem + L::OFF_STAT + st * 1024 + 512, p.dd + ws, 512, &q_full[st]);
-        *issued = t + 1;
+        *issued_q = t + 1;
+        if (t >= STAGES && !mbar_wait(&do_empty[st], eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(&do_full[st], L::TILE);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(smem + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, &do_full[st], kb * 64, q0, bh);
+        *issued_do = t + 1;
       }
     }
   } else if (warp == 1) {
@@ -307,22 +318,27 @@ __global__ void __launch_bounds__(384, 1)
                   kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(kv_full, 0, wc, ST_BWD_TIMEOUT_KV);
-      for (int t = 0; ok && t < n_it; ++t) {
-        const int st = t % STAGES;
-        const uint32_t ph = t & 1;
-        const uint32_t q_t = sq + st * L::TILE, do_t = sdo + st * L::TILE;
-        // MMA1: S^T_t.  The S columns are free: P_{t-1} was read by MMA3_{t-1},
-        // issued earlier (the tensor cores run in issue order).
-        if (!mbar_wait(&q_full[st], (t / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q)) break;
+      // Issue order: MMA1_0, MMA2_0, then per tile t
+      //   MMA3_t, MMA1_{t+1}, MMA4_t, MMA5_t, MMA2_{t+1}
+      // so that S^T_{t+1} is ready while the warpgroups finish tile t, and
+      // MMA4_t / MMA5_t run while they form P^T_{t+1}.
+      bool ok = mbar_wait(kv_full, 0, wc, ST_BWD_TIMEOUT_KV) && mbar_wait(&q_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
+      if (ok) {
         tc_fence_after();
-        mma_scores(tmem + L::TM_S, sk, q_t);
+        mma_scores(tmem + L::TM_S, sk, sq);
         umma_commit(s_full);
-        // MMA2: dP^T_t, into the columns dQ^T_{t-1} occupied until drained
-        if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) break;
+        ok = mbar_wait(&do_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
+      }
+      if (ok) {
         tc_fence_after();
-        mma_scores(tmem + L::TM_DP, sv, do_t);
+        mma_scores(tmem + L::TM_DP, sv, sdo);
         umma_commit(dp_full);
+      }
+      for (int t = 0; ok && t < n_it; ++t) {
+        const int st = t % STAGES, st1 = (t + 1) % STAGES;
+        const uint32_t ph = t & 1, ph1 = ((t + 1) / STAGES) & 1;
+        const uint32_t q_t = sq + st * L::TILE, do_t = sdo + st * L::TILE;
+        const bool next = t + 1 < n_it;
         // MMA3: dV += P^T_t dO_t.  A = P^T from tensor memory: queries 0-63 in
         // columns [0, 32), queries 64-127 in [64, 96) (each half in its own
         // S columns); B = dO_t MN-major (16 queries = 2 KB per step).
@@ -334,29 +350,68 @@ __global__ void __launch_bounds__(384, 1)
           umma_ts(tmem + L::TM_DV, tmem + L::TM_S + pcol, sdesc_sw128(do_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
                   (t > 0 || kk > 0) ? 1u : 0u);
         }
-        // MMA5: dQ^T_t = K^T dS_t into the dP columns (dP_t was read before dS_t
-        // was published).  A = K MN-major, B = dS^T read as [query][key] MN-major
-        // (two 64-query blocks, 16 KB apart).
+        // MMA1: S^T_{t+1} into the S columns.  P^T_t is read by MMA3_t, issued
+        // just before (the tensor cores run in issue order).
+        if (next) {
+          if (!mbar_wait(&q_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          tc_fence_after();
+          mma_scores(tmem + L::TM_S, sk, sq + st1 * L::TILE);
+          umma_commit(s_full);
+        }
         if (!mbar_wait(ds_full, ph, wc, ST_BWD_TIMEOUT_DS)) break;
         tc_fence_after();
+        // MMA4: dK += dS^T_t Q_t.  A = dS^T (bf16) from the dP columns, laid out
+        // like P^T; B = Q_t MN-major.
+#pragma unroll
+        for (int kk = 0; kk < L::BM / 16; ++kk) {
+          const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_ts(tmem + L::TM_DK, tmem + L::TM_DP + pcol, sdesc_sw128(q_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
+                  (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&q_empty[st]);
+        // MMA5: dQ^T_t = K^T dS_t into the dP columns, after MMA4 has read dS^T
+        // there.  A = K MN-major, B = dS^T read as [query][key] MN-major (two
+        // 64-query blocks, 16 KB apart).
 #pragma unroll
         for (int kk = 0; kk < L::BN / 16; ++kk)
           umma_ss(tmem + L::TM_DP, sdesc_sw128(sk + kk * 2048, L::COLBLK, 1024),
                   sdesc_sw128(sds + kk * 2048, L::COLBLK, 1024), IDESC_Q, kk > 0 ? 1u : 0u);
-        umma_commit(dq_full);
-        // MMA4: dK += dS^T_t Q_t.  A = dS^T K-major (two 64-query blocks), B = Q_t MN-major.
-#pragma unroll
-        for (int kk = 0; kk < L::BM / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
-          umma_ss(tmem + L::TM_DK, sdesc_sw128(sds + off, 16, 1024), sdesc_sw128(q_t + kk * 2048, L::COLBLK, 1024),
-                  IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(dq_full);  // also MMA4_t: dO_t's buffer and the dS buffer are free
+        // MMA2: dP^T_{t+1} into the dP columns once dQ^T_t has been drained
+        if (next) {
+          if (!mbar_wait(dq_empty, ph, wc, ST_BWD_TIMEOUT_DQE)) break;
+          if (!mbar_wait(&do_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          tc_fence_after();
+          mma_scores(tmem + L::TM_DP, sv, sdo + st1 * L::TILE);
+          umma_commit(dp_full);
         }
-        umma_commit(&stage_done[st]);  // Q_t and dO_t are no longer read by the tensor cores
       }
       umma_commit(dkv_done);
       // nothing may be in flight on the tensor cores when the CTA frees TMEM
       umma_commit(drain);
       if (!mbar_wait_drain(drain, 0, DRAIN_NS)) atomicOr(p.status, ST_DRAIN);
+    }
+  } else if (warp == 2) {
+    // ----------------------------------------------------- dQ reduce-adds --
+    // Per tile: the half staged in the dS buffer first (the warpgroups need the
+    // buffer back for dS^T_{t+1}), then the half in dO_t's buffer.
+    if (lane == 0 && n_it > 0) {
+      for (int t = 0; t < n_it; ++t) {
+        const int st = t % STAGES;
+        const int q0 = (i0 + t) * L::BM;
+        if (!mbar_wait(&red_ready[1], t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
+        tma_reduce_add_3d(&tm_dq, smem + L::OFF_DS, 0, q0 + 64, bh);
+        bulk_commit_group();
+        if (!mbar_wait(&red_ready[0], t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
+        tma_reduce_add_3d(&tm_dq, smem + L::OFF_DO + st * L::TILE, 0, q0, bh);
+        bulk_commit_group();
+        bulk_wait_read<1>();
+        mbar_arrive(ds_free);
+        bulk_wait_read<0>();
+        mbar_arrive(&do_empty[st]);
+      }
+      // the CTA may not exit while a reduce-add still reads its shared memory
+      bulk_wait_all();
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------- elementwise WGs --
@@ -371,133 +426,129 @@ __global__ void __launch_bounds__(384, 1)
     const bool key_ok = (k0 + r) < kv_limit;
     const float sl = p.scale_log2, scale = p.scale;
     const uint32_t ds_row = smem_u32(smem + L::OFF_DS) + h * L::COLBLK + r * 128;
-    const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + st * 1024: lse2; + 512: D
-    // dQ staging: warpgroup 0 reuses the stage's Q buffer, warpgroup 1 its dO buffer
-    uint8_t* const stage_out = smem + (h == 0 ? L::OFF_Q : L::OFF_DO);
-    const bool leader = (r == 0);  // issues this warpgroup's dQ reduce-adds
-    int pending = -1;              // stage whose reduce-add the leader has not yet released
+    const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + stage * 1024: lse2; + 512: D
     bool ok = true;
-    for (int t = 0; t < n_it; ++t) {
-      const int st = t % STAGES;
-      const uint32_t ph = t & 1, sph = (t / STAGES) & 1;
-      const int q0 = (i0 + t) * L::BM + h * 64;  // first query of this half
-      // q_full is already complete here (S^T_t exists); waiting on it makes the
-      // stage's lse2 / D rows visible to these threads
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, ph, wc, ST_BWD_TIMEOUT_S) &&
-                                       mbar_wait(&q_full[st], sph, wc, ST_BWD_TIMEOUT_Q))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[64];
-      FA_TMEM_LD32(s_col + 0, sr + 0);
-      FA_TMEM_LD32(s_col + 32, sr + 32);
-      tmem_wait_ld();
-      FA_REG_FENCE32(sr + 0);
-      FA_REG_FENCE32(sr + 32);
-      // causal: key k0 + r is visible to query q0 + j iff j >= r - (q0 - k0),
-      // one later in the strict mode (a query does not see its own key)
-      const int jmin = p.causal ? r - (q0 - k0) + (p.causal == 2 ? 1 : 0) : -1;
-      const uint32_t lse2_s = stat + st * 1024, dd_s = lse2_s + 512;
-      float pr[64];
-#pragma unroll
-      for (int j4 = 0; j4 < 64; j4 += 4) {
-        float lv[4];
-        ld_shared_v4f(lse2_s + j4 * 4, lv);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = j4 + u;
-          const float e = ex2_approx(fmaf(__uint_as_float(sr[j]), sl, -lv[u]));
-          pr[j] = (key_ok && j >= jmin) ? e : 0.f;
+    float pr[64];
+    // Pass t forms P^T and dS^T of tile u = t + 1 around the drain of dQ^T_t:
+    //   P^T_u  |  dQ^T_t -> staged row-major for its reduce-add  |  dS^T_u
+    for (int t = -1; t < n_it; ++t) {
+      const int u = t + 1;
+      const int su = u % STAGES;
+      const int qu = (i0 + u) * L::BM + h * 64;  // first query of this half of tile u
+      if (u < n_it) {
+        // q_full is already complete here (S^T_u exists); waiting on it makes the
+        // stage's lse2 / D rows visible to these threads
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full, u & 1, wc, ST_BWD_TIMEOUT_S) &&
+                                         mbar_wait(&q_full[su], (u / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
+          ok = false;
+          break;
         }
-      }
-      uint32_t pk[32];
+        tc_fence_after();
+        // causal: key k0 + r is visible to query qu + j iff j >= r - (qu - k0),
+        // one later in the strict mode (a query does not see its own key)
+        const int jmin = p.causal ? r - (qu - k0) + (p.causal == 2 ? 1 : 0) : -1;
+        const uint32_t lse2_s = stat + su * 1024;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
-      FA_TMEM_ST32(s_col, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
-      // the previous tile's reduce-add has had the P phase to read its source
-      if (leader && pending >= 0) {
-        bulk_wait_read_all();
-        mbar_arrive(&q_empty[pending]);
-        pending = -1;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sr[32];
+          FA_TMEM_LD32(s_col + half * 32, sr);
+          tmem_wait_ld();
+          FA_REG_FENCE32(sr);
+#pragma unroll
+          for (int j4 = 0; j4 < 32; j4 += 4) {
+            float lv[4];
+            ld_shared_v4f(lse2_s + (half * 32 + j4) * 4, lv);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int j = half * 32 + j4 + w;
+              const float e = ex2_approx(fmaf(__uint_as_float(sr[j4 + w]), sl, -lv[w]));
+              pr[j] = (key_ok && j >= jmin) ? e : 0.f;
+            }
+          }
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+        FA_TMEM_ST32(s_col, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
 
-      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, ph, wc, ST_BWD_TIMEOUT_DP))) {
-        ok = false;
-        break;
+      if (t >= 0) {
+        // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows.
+        // Stage them row-major -- warpgroup 0 in dO_t's buffer, warpgroup 1 in
+        // the dS buffer, both free once MMA5_t (the last MMA of tile t) has run --
+        // for one tiled reduce-add into global dQ (rows past N are skipped by
+        // the tensor map).  A warp's 32 lanes write 128 consecutive bytes per
+        // store.  32 columns at a time keeps P^T_u's registers live alongside.
+        if (!__all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, wc, ST_BWD_TIMEOUT_DQ))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t out_row =
+            smem_u32(smem + (h == 0 ? L::OFF_DO + (t % STAGES) * L::TILE : L::OFF_DS)) + r * 4;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t qr[32];
+          FA_TMEM_LD32(dp_col + half * 32, qr);
+          tmem_wait_ld();
+          FA_REG_FENCE32(qr);
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) st_shared_f32(out_row + (half * 32 + j) * 512, __uint_as_float(qr[j]));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&red_ready[h]);
       }
-      tc_fence_after();
-      uint32_t dpr[64];
-      FA_TMEM_LD32(dp_col + 0, dpr + 0);
-      FA_TMEM_LD32(dp_col + 32, dpr + 32);
-      tmem_wait_ld();
-      FA_REG_FENCE32(dpr + 0);
-      FA_REG_FENCE32(dpr + 32);
-      uint32_t dsk[32];
-#pragma unroll
-      for (int j4 = 0; j4 < 64; j4 += 4) {
-        float dv4[4];
-        ld_shared_v4f(dd_s + j4 * 4, dv4);
-        float g[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) g[u] = pr[j4 + u] * (__uint_as_float(dpr[j4 + u]) - dv4[u]) * scale;
-        dsk[j4 / 2] = pack_bf16x2(g[0], g[1]);
-        dsk[j4 / 2 + 1] = pack_bf16x2(g[2], g[3]);
-      }
-      // Row r of this half's 128B-swizzled block: 16-byte chunk c lands at c ^ (r & 7).
-      // The block is free: MMA4/MMA5 of the previous tile finished before s_full
-      // (issued after them) completed.
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(ds_full);
 
-      // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows
-      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, ph, wc, ST_BWD_TIMEOUT_DQ))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t qr[64];
-      FA_TMEM_LD32(dp_col + 0, qr + 0);
-      FA_TMEM_LD32(dp_col + 32, qr + 32);
-      tmem_wait_ld();
-      FA_REG_FENCE32(qr + 0);
-      FA_REG_FENCE32(qr + 32);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      // Stage the 64 x d block row-major in the stage's Q (dO) buffer, free once
-      // MMA4_t has run, and add it into global dQ with one tiled reduce-add;
-      // rows past N are skipped by the tensor map.  A warp's 32 lanes write 128
-      // consecutive bytes per store.
-      if (!__all_sync(0xffffffffu, mbar_wait(&stage_done[st], sph, wc, ST_BWD_TIMEOUT_EMPTY))) {
-        ok = false;
-        break;
-      }
-      const uint32_t out_row = smem_u32(stage_out + st * L::TILE) + r * 4;
+      if (u < n_it) {
+        if (!__all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, wc, ST_BWD_TIMEOUT_DP))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dd_s = stat + su * 1024 + 512;
+        uint32_t dsk[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) st_shared_f32(out_row + j * 512, __uint_as_float(qr[j]));
-      fence_proxy_async_smem();
-      mbar_arrive(&red_ready[h]);
-      if (!__all_sync(0xffffffffu, !leader || mbar_wait(&red_ready[h], ph, wc, ST_BWD_TIMEOUT_RED))) {
-        ok = false;
-        break;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t dpr[32];
+          FA_TMEM_LD32(dp_col + half * 32, dpr);
+          tmem_wait_ld();
+          FA_REG_FENCE32(dpr);
+#pragma unroll
+          for (int j4 = 0; j4 < 32; j4 += 4) {
+            const int j = half * 32 + j4;
+            float dv4[4];
+            ld_shared_v4f(dd_s + j * 4, dv4);
+            float g[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) g[w] = pr[j + w] * (__uint_as_float(dpr[j4 + w]) - dv4[w]) * scale;
+            dsk[j / 2] = pack_bf16x2(g[0], g[1]);
+            dsk[j / 2 + 1] = pack_bf16x2(g[2], g[3]);
+          }
+        }
+        // The dS buffer is free once the dQ^T_t half staged there has been read.
+        if (t >= 0 && !__all_sync(0xffffffffu, mbar_wait(ds_free, t & 1, wc, ST_BWD_TIMEOUT_RED))) {
+          ok = false;
+          break;
+        }
+        // dS^T as MMA4's A operand: bf16 pairs into the first 32 of this half's
+        // dP columns (dP^T has been read into registers)
+        FA_TMEM_ST32(dp_col, dsk);
+        // Row r of this half's 128B-swizzled block: 16-byte chunk c lands at c ^ (r & 7).
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(ds_full);
       }
-      if (leader) {
-        tma_reduce_add_3d(&tm_dq, stage_out + st * L::TILE, 0, q0, bh);
-        bulk_commit_group();
-        pending = st;
-      }
-    }
-    if (leader) {
-      // the CTA may not exit while a reduce-add still reads its shared memory
-      bulk_wait_all();
-      if (pending >= 0) mbar_arrive(&q_empty[pending]);
     }
 
     // ------------------------------------------------------------ epilogue --
@@ -535,9 +586,11 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 && lane == 0 && n_it > 0 && *abort_flag) {
     // an aborted CTA may not exit while copies it issued are still landing
     bool ok = mbar_wait_drain(kv_full, 0, DRAIN_NS);
-    const int n_iss = *issued;
-    for (int t = max(0, n_iss - STAGES); t < n_iss; ++t)
+    const int nq = *issued_q, nd = *issued_do;
+    for (int t = max(0, nq - STAGES); t < nq; ++t)
       ok &= mbar_wait_drain(&q_full[t % STAGES], (t / STAGES) & 1, DRAIN_NS);
+    for (int t = max(0, nd - STAGES); t < nd; ++t)
+      ok &= mbar_wait_drain(&do_full[t % STAGES], (t / STAGES) & 1, DRAIN_NS);
     if (!ok) atomicOr(p.status, ST_DRAIN);
   }
   if (warp == 1) {
