@@ -15,38 +15,42 @@
 //    (row stride Np = N rounded up to 128; padding rows get D = 0, lse2 = +inf so
 //    that their probabilities are exactly 0), and zeroes dQ.
 //  * bwd_bf16_tc_kernel -- one CTA per (batch, head, 128-key tile).  K and V stay
-//    in shared memory; the CTA streams 64-query tiles (Q_t, dO_t, lse2_t, D_t)
-//    through a TMA ring and, per tile t, runs five MMAs:
-//       MMA1  S^T_t  = K Q_t^T            (128 x 64, TMEM)
-//       MMA2  dP^T_t = V dO_t^T           (128 x 64, TMEM)
-//       MMA3  dV    += P^T_t dO_t          (128 x d, TMEM; A = P^T from TMEM)
-//       MMA4  dK    += dS^T_t Q_t          (128 x d, TMEM; A = dS^T from SMEM)
-//       MMA5  dQ^T_t = K^T dS_t            (d x 64, TMEM; A = K read MN-major)
-//    issued in the order MMA3_t, MMA1_{t+1}, MMA2_{t+1}, MMA4_t, MMA5_t so that
-//    the next tile's products are queued while tile t's softmax runs.
-//    dQ is produced transposed so that TMEM lane = head-dim column: a warp's 32
-//    lanes then hold 32 consecutive floats of one query row, and the reduction
-//    into global dQ (red.global.add.f32) is one coalesced 128-byte access per
-//    warp instruction.  dS carries the factor `scale`, so dK and dQ need no
-//    further scaling.
+//    in shared memory; the CTA streams 128-query tiles (Q_t with its lse2_t and
+//    D_t rows, and dO_t) through a 2-stage TMA ring and, per tile t, runs five
+//    MMAs (128 x 128 x 128 each):
+//       MMA1  S^T_t  = K Q_t^T            (A = K, B = Q_t, both from SMEM)
+//       MMA2  dP^T_t = V dO_t^T           (A = V, B = dO_t)
+//       MMA3  dV    += P^T_t dO_t          (A = P^T from TMEM, B = dO_t MN-major)
+//       MMA4  dK    += dS^T_t Q_t          (A = dS^T from TMEM, B = Q_t MN-major)
+//       MMA5  dQ^T_t = K^T dS_t            (A = K MN-major, B = dS^T MN-major, SMEM)
+//    issued as MMA3_t, MMA1_{t+1}, MMA4_t, MMA5_t, MMA2_{t+1}: S^T of the next
+//    tile is ready while tile t finishes, and dK / dQ of tile t run while the
+//    elementwise warps form P^T_{t+1}.  dS carries the factor `scale`, so dK and
+//    dQ need no further scaling.
+//    dQ^T_t is staged row-major in shared memory (the dO_t buffer and the dS
+//    buffer, both free once MMA5_t has run) and added into global dQ with two
+//    tiled TMA reduce-adds (cp.reduce.async.bulk.tensor .add.f32), which skip
+//    the rows past N.
 //
 // Roles (384 threads):
-//   warp 0     TMA producer: K, V once; then Q_t, dO_t (tensor maps) and the
-//              lse2_t, D_t rows (bulk copies) into a STAGES-deep ring.
+//   warp 0     TMA producer: K, V once; then Q_t + lse2_t + D_t and dO_t into the
+//              ring (separate full / empty barriers for Q and dO).
 //   warp 1     MMA issuer (one thread) and tensor-memory owner.
-//   warps 4-7  elementwise warpgroup 0: even tiles t;  warps 8-11: odd tiles.
+//   warp 2     dQ reducer: issues the reduce-adds once a half is staged and
+//              hands the buffers back when the copies have read them.
+//   warps 4-7  elementwise warpgroup 0, query columns 0-63 of every tile;
+//   warps 8-11 elementwise warpgroup 1, query columns 64-127.
 //              Thread r owns key row r (TMEM lane r) of S^T and dP^T:
 //                P^T = 2^(S^T scale log2e - lse2) with the causal / padding mask,
-//                written back to TMEM as bf16 (aliasing S^T), then
-//                dS^T = P^T (dP^T - D) scale -> bf16, 128B-swizzled into SMEM,
-//              and, as TMEM lane r of dQ^T, adds head-dim column r of the tile's
-//              64 dQ rows into global memory.  At the end warpgroup 0 writes dV
-//              and warpgroup 1 writes dK.
+//                written back to TMEM as bf16 (aliasing S^T); then
+//                dS^T = P^T (dP^T - D) scale -> bf16, into TMEM (aliasing dP^T,
+//                for MMA4) and 128B-swizzled into SMEM (for MMA5); and, as TMEM
+//                lane r of dQ^T, stages head-dim column r of its 64 dQ rows.
+//              At the end warpgroup 0 writes dV and warpgroup 1 writes dK.
 //
 // Tensor memory (512 columns, f32 unless noted):
-//   [0,128)   two 64-column buffers, one per tile parity: S^T_t, then P^T_t
-//             (bf16, first 32 columns), then dQ^T_t
-//   [128,256) two dP^T buffers, one per tile parity
+//   [0,128)   S^T_t, then P^T_t (bf16: queries 0-63 in [0,32), 64-127 in [64,96))
+//   [128,256) dP^T_t, then dS^T_t (bf16, same layout as P^T), then dQ^T_t
 //   [256,384) dV   [384,512) dK
 //
 // Every wait is bounded, as in the forward kernel: a wait that runs out records
