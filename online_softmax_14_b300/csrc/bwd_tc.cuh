@@ -35,7 +35,7 @@
 // Roles (384 threads):
 //   warp 0     TMA producer: K, V once; then Q_t + lse2_t + D_t and dO_t into the
 //              ring (separate full / empty barriers for Q and dO).
-//   warp 1     MMA issuer (one thread) and tensor-memory owner.
+//   warp 1     MMA issuer (lane 0 of the converged warp) and tensor-memory owner.
 //   warp 2     dQ reducer: issues the reduce-adds once a half is staged and
 //              hands the buffers back when the copies have read them.
 //   warps 4-7  elementwise warpgroup 0, query columns 0-63 of every tile;
@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0 && n_it > 0) {
+    // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
+    if (n_it > 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, L::BM, false, false);  // K Q^T, V dO^T
       constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, true, false);       // P^T dO, dS^T Q
       constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, L::BM, true, true);      // K^T dS
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
-          umma_ss(d_tm, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), IDESC_S,
+          umma_ss_w(d_tm, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), IDESC_S,
                   kk > 0 ? 1u : 0u);
         }
       };
@@ -326,17 +327,17 @@ __global__ void __launch_bounds__(384, 1)
       //   MMA3_t, MMA1_{t+1}, MMA4_t, MMA5_t, MMA2_{t+1}
       // so that S^T_{t+1} is ready while the warpgroups finish tile t, and
       // MMA4_t / MMA5_t run while they form P^T_{t+1}.
-      bool ok = mbar_wait(kv_full, 0, wc, ST_BWD_TIMEOUT_KV) && mbar_wait(&q_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
+      bool ok = mbar_wait_w(kv_full, 0, wc, ST_BWD_TIMEOUT_KV) && mbar_wait_w(&q_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
       if (ok) {
         tc_fence_after();
         mma_scores(tmem + L::TM_S, sk, sq);
-        umma_commit(s_full);
-        ok = mbar_wait(&do_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
+        umma_commit_w(s_full);
+        ok = mbar_wait_w(&do_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
       }
       if (ok) {
         tc_fence_after();
         mma_scores(tmem + L::TM_DP, sv, sdo);
-        umma_commit(dp_full);
+        umma_commit_w(dp_full);
       }
       for (int t = 0; ok && t < n_it; ++t) {
         const int st = t % STAGES, st1 = (t + 1) % STAGES;
@@ -346,54 +347,54 @@ __global__ void __launch_bounds__(384, 1)
         // MMA3: dV += P^T_t dO_t.  A = P^T from tensor memory: queries 0-63 in
         // columns [0, 32), queries 64-127 in [64, 96) (each half in its own
         // S columns); B = dO_t MN-major (16 queries = 2 KB per step).
-        if (!mbar_wait(p_full, ph, wc, ST_BWD_TIMEOUT_P)) break;
+        if (!mbar_wait_w(p_full, ph, wc, ST_BWD_TIMEOUT_P)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < L::BM / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_ts(tmem + L::TM_DV, tmem + L::TM_S + pcol, sdesc_sw128(do_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
+          umma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + pcol, sdesc_sw128(do_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
                   (t > 0 || kk > 0) ? 1u : 0u);
         }
         // MMA1: S^T_{t+1} into the S columns.  P^T_t is read by MMA3_t, issued
         // just before (the tensor cores run in issue order).
         if (next) {
-          if (!mbar_wait(&q_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          if (!mbar_wait_w(&q_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
           tc_fence_after();
           mma_scores(tmem + L::TM_S, sk, sq + st1 * L::TILE);
-          umma_commit(s_full);
+          umma_commit_w(s_full);
         }
-        if (!mbar_wait(ds_full, ph, wc, ST_BWD_TIMEOUT_DS)) break;
+        if (!mbar_wait_w(ds_full, ph, wc, ST_BWD_TIMEOUT_DS)) break;
         tc_fence_after();
         // MMA4: dK += dS^T_t Q_t.  A = dS^T (bf16) from the dP columns, laid out
         // like P^T; B = Q_t MN-major.
 #pragma unroll
         for (int kk = 0; kk < L::BM / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_ts(tmem + L::TM_DK, tmem + L::TM_DP + pcol, sdesc_sw128(q_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
+          umma_ts_w(tmem + L::TM_DK, tmem + L::TM_DP + pcol, sdesc_sw128(q_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
                   (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&q_empty[st]);
+        umma_commit_w(&q_empty[st]);
         // MMA5: dQ^T_t = K^T dS_t into the dP columns, after MMA4 has read dS^T
         // there.  A = K MN-major, B = dS^T read as [query][key] MN-major (two
         // 64-query blocks, 16 KB apart).
 #pragma unroll
         for (int kk = 0; kk < L::BN / 16; ++kk)
-          umma_ss(tmem + L::TM_DP, sdesc_sw128(sk + kk * 2048, L::COLBLK, 1024),
+          umma_ss_w(tmem + L::TM_DP, sdesc_sw128(sk + kk * 2048, L::COLBLK, 1024),
                   sdesc_sw128(sds + kk * 2048, L::COLBLK, 1024), IDESC_Q, kk > 0 ? 1u : 0u);
-        umma_commit(dq_full);  // also MMA4_t: dO_t's buffer and the dS buffer are free
+        umma_commit_w(dq_full);  // also MMA4_t: dO_t's buffer and the dS buffer are free
         // MMA2: dP^T_{t+1} into the dP columns once dQ^T_t has been drained
         if (next) {
-          if (!mbar_wait(dq_empty, ph, wc, ST_BWD_TIMEOUT_DQE)) break;
-          if (!mbar_wait(&do_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          if (!mbar_wait_w(dq_empty, ph, wc, ST_BWD_TIMEOUT_DQE)) break;
+          if (!mbar_wait_w(&do_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
           tc_fence_after();
           mma_scores(tmem + L::TM_DP, sv, sdo + st1 * L::TILE);
-          umma_commit(dp_full);
+          umma_commit_w(dp_full);
         }
       }
-      umma_commit(dkv_done);
+      umma_commit_w(dkv_done);
       // nothing may be in flight on the tensor cores when the CTA frees TMEM
-      umma_commit(drain);
-      if (!mbar_wait_drain(drain, 0, DRAIN_NS)) atomicOr(p.status, ST_DRAIN);
+      umma_commit_w(drain);
+      if (!mbar_wait_drain(drain, 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
     }
   } else if (warp == 2) {
     // ----------------------------------------------------- dQ reduce-adds --

@@ -22,7 +22,7 @@
 //   warps 0-3   softmax of tile 0: thread r owns row r = tensor-memory lane r
 //   warps 4-7   softmax of tile 1
 //   warp 8      TMA producer: Q0, Q1 once, then K_j, V_j through a ring of NS slots
-//   warp 9      MMA issuer (one thread) and tensor-memory owner
+//   warp 9      MMA issuer (lane 0 of the converged warp) and tensor-memory owner
 //
 // Tensor memory (512 columns, f32 unless noted):
 //   [0,128) S0, then P0 (bf16 pairs in its first 64 columns)   [128,256) S1 / P1
@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0 && n_max > 0) {
+    // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
+    if (n_max > 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, true);
       const uint32_t sq = smem_u32(smem + L::OFF_Q);
@@ -206,9 +207,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
-          umma_ss(tm_s, qa + off, ka + off, IDESC_QK, kk > 0 ? 1u : 0u);
+          umma_ss_w(tm_s, qa + off, ka + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar);
+        umma_commit_w(bar);
       };
       // O_i += P_i V_j.  Only the tile's last product signals o_done (for the
       // epilogue): an earlier PV_i(j-1) is known complete once S_i(j), issued
@@ -218,18 +219,18 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t va = dv_base + ((((2 * j + 1) % NS) * L::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < L::BN / 16; ++kk)
-          umma_ts(tm_o, tm_p + kk * 8, va + (kk * 2048 >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        if (last) umma_commit(bar);
+          umma_ts_w(tm_o, tm_p + kk * 8, va + (kk * 2048 >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        if (last) umma_commit_w(bar);
       };
       const uint32_t tS0 = tmem + L::TM_S0, tS1 = tmem + L::TM_S1;
       const uint32_t tO0 = tmem + L::TM_O0, tO1 = tmem + L::TM_O1;
 
-      bool ok = mbar_wait(q_full, 0, wc, ST_TIMEOUT_Q) && mbar_wait(&kv_full[0], 0, wc, ST_TIMEOUT_K);
+      bool ok = mbar_wait_w(q_full, 0, wc, ST_TIMEOUT_Q) && mbar_wait_w(&kv_full[0], 0, wc, ST_TIMEOUT_K);
       if (ok) {
         tc_fence_after();
         if (n_t0 > 0) issue_s(tS0, 0, &s_full[0], 0);
         if (n_t1 > 0) issue_s(tS1, L::TILE, &s_full[1], 0);
-        umma_commit(&kv_empty[0]);
+        umma_commit_w(&kv_empty[0]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
         const int j1 = j + 1;
@@ -238,18 +239,18 @@ __global__ void __launch_bounds__(384, 1)
         bool k1_ready = false, v_ready = false;
         auto wait_v = [&]() -> bool {
           if (v_ready) return true;
-          v_ready = mbar_wait(&kv_full[cv % NS], (cv / NS) & 1, wc, ST_TIMEOUT_V);
+          v_ready = mbar_wait_w(&kv_full[cv % NS], (cv / NS) & 1, wc, ST_TIMEOUT_V);
           return v_ready;
         };
         auto wait_k1 = [&]() -> bool {
           if (k1_ready) return true;
-          k1_ready = mbar_wait(&kv_full[ck % NS], (ck / NS) & 1, wc, ST_TIMEOUT_K);
+          k1_ready = mbar_wait_w(&kv_full[ck % NS], (ck / NS) & 1, wc, ST_TIMEOUT_K);
           if (k1_ready) tc_fence_after();
           return k1_ready;
         };
         // tile 0: PV0_j, then S0_{j+1}
         if (j < n_t0) {
-          if (!wait_v() || !mbar_wait(&p_full[0], j & 1, wc, ST_TIMEOUT_P)) break;
+          if (!wait_v() || !mbar_wait_w(&p_full[0], j & 1, wc, ST_TIMEOUT_P)) break;
           tc_fence_after();
           issue_pv(tO0, tS0, &o_done[0], j, j + 1 == n_t0);
         }
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         // tile 1: PV1_j, then S1_{j+1}
         if (j < n_t1) {
-          if (!wait_v() || !mbar_wait(&p_full[1], j & 1, wc, ST_TIMEOUT_P)) break;
+          if (!wait_v() || !mbar_wait_w(&p_full[1], j & 1, wc, ST_TIMEOUT_P)) break;
           tc_fence_after();
           issue_pv(tO1, tS1, &o_done[1], j, j + 1 == n_t1);
         }
@@ -267,12 +268,12 @@ __global__ void __launch_bounds__(384, 1)
           if (!wait_k1()) break;
           issue_s(tS1, L::TILE, &s_full[1], j1);
         }
-        umma_commit(&kv_empty[cv % NS]);                 // V_j: read by every PV above
-        if (j1 < n_max) umma_commit(&kv_empty[ck % NS]);  // K_{j+1}: read by every S above
+        umma_commit_w(&kv_empty[cv % NS]);                 // V_j: read by every PV above
+        if (j1 < n_max) umma_commit_w(&kv_empty[ck % NS]);  // K_{j+1}: read by every S above
       }
       // nothing may be in flight on the tensor cores when the CTA frees TMEM
-      umma_commit(drain);
-      if (!mbar_wait_drain(drain, 0, DRAIN_NS)) atomicOr(p.status, ST_DRAIN);
+      umma_commit_w(drain);
+      if (!mbar_wait_drain(drain, 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------- softmax --

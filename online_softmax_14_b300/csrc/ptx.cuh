@@ -74,6 +74,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// mbar_wait for a whole converged warp: every lane tests the barrier and the
+// outcome is made warp-uniform (a phase, once complete, stays complete).
+__device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, const WaitCtl& w, unsigned code) {
+  const uint32_t a = smem_u32(bar);
+  if (__any_sync(0xffffffffu, mbar_try_wait(a, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (__any_sync(0xffffffffu, mbar_try_wait(a, parity))) return true;
+    if ((it & 63u) == 0u) {
+      if (__any_sync(0xffffffffu, *w.abort_flag != 0)) return false;
+      if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > w.timeout_ns)) {
+        if ((threadIdx.x & 31) == 0) {
+          *w.abort_flag = 1;
+          atomicOr(w.status, code);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // Wait with a limit, ignoring the abort flag: used only while draining work that
 // is already in flight before a CTA exits.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -200,6 +221,40 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// Warp-converged issue.  All 32 lanes of the issuing warp run the issue code
+// (the operands are warp-uniform) and lane 0 alone executes the tensor-core
+// instruction through a predicate.  Measured on B300: a barrier test between two
+// groups of MMAs stalls the tensor pipe for ~190 cycles when one lane runs the
+// issue code on its own, and for ~20 cycles when the warp stays converged.
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Lane 0 (the lane that issued the MMAs) commits them to `bar`.
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 
 // Instruction descriptor, kind::f16 with bf16 A and B, f32 accumulator.
