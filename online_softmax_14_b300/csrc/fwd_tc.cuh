@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(384, 1)
       // sum in 4 independent chains; P in quarters of 32 scores (16 packed
       // columns) keeps register use low
       const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_ref, -m_ref);
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      // row sum in two f32x2 chains: one packed add per pair of scores
+      uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
@@ -345,12 +346,15 @@ __global__ void __launch_bounds__(384, 1)
                            sl2, nm2),
                     x0, x1);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          rs4[i & 3] += p0 + p1;
+          rs2[i & 1] = f2_add(rs2[i & 1], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         FA_TMEM_ST16(s_col + 16 * h, pk);
       }
-      l = l * c + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      float ra, rb, rc, rd;
+      f2_unpack(rs2[0], ra, rb);
+      f2_unpack(rs2[1], rc, rd);
+      l = l * c + ((ra + rb) + (rc + rd));
       if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
         // The accumulator already holds blocks < j: PV_{j-1} was issued before
         // S_j, and s_full for S_j tracks every earlier tensor-core operation.
