@@ -11,12 +11,14 @@
 // already normalised, so no second softmax pass is needed.
 //
 // Two kernels:
-//  * bwd_preprocess_kernel -- D_i and lse2_i = lse_i log2(e) into the workspace
-//    (row stride Np = N rounded up to 128; padding rows get D = 0, lse2 = +inf so
-//    that their probabilities are exactly 0), and zeroes dQ.
+//  * bwd_preprocess_kernel -- nl_i = -lse_i log2(e) and nd_i = -D_i scale into
+//    the workspace (row stride Np = N rounded up to 128; padding rows get nl =
+//    -inf, so that their probabilities are exactly 0, and nd = 0), and zeroes dQ.
+//    With them P^T = 2^(S^T scale log2e + nl) and dS^T = P^T (dP^T scale + nd)
+//    take one packed FMA (and one packed multiply) per pair of entries.
 //  * bwd_bf16_tc_kernel -- one CTA per (batch, head, 128-key tile).  K and V stay
-//    in shared memory; the CTA streams 128-query tiles (Q_t with its lse2_t and
-//    D_t rows, and dO_t) through a 2-stage TMA ring and, per tile t, runs five
+//    in shared memory; the CTA streams 128-query tiles (Q_t with its nl_t and
+//    nd_t rows, and dO_t) through a 2-stage TMA ring and, per tile t, runs five
 //    MMAs (128 x 128 x 128 each):
 //       MMA1  S^T_t  = K Q_t^T            (A = K, B = Q_t, both from SMEM)
 //       MMA2  dP^T_t = V dO_t^T           (A = V, B = dO_t)
@@ -33,7 +35,7 @@
 //    the rows past N.
 //
 // Roles (384 threads):
-//   warp 0     TMA producer: K, V once; then Q_t + lse2_t + D_t and dO_t into the
+//   warp 0     TMA producer: K, V once; then Q_t + nl_t + nd_t and dO_t into the
 //              ring (separate full / empty barriers for Q and dO).
 //   warp 1     MMA issuer (lane 0 of the converged warp) and tensor-memory owner.
 //   warp 2     dQ reducer: issues the reduce-adds once a half is staged and
@@ -41,9 +43,9 @@
 //   warps 4-7  elementwise warpgroup 0, query columns 0-63 of every tile;
 //   warps 8-11 elementwise warpgroup 1, query columns 64-127.
 //              Thread r owns key row r (TMEM lane r) of S^T and dP^T:
-//                P^T = 2^(S^T scale log2e - lse2) with the causal / padding mask,
+//                P^T = 2^(S^T scale log2e + nl) with the causal / padding mask,
 //                written back to TMEM as bf16 (aliasing S^T); then
-//                dS^T = P^T (dP^T - D) scale -> bf16, into TMEM (aliasing dP^T,
+//                dS^T = P^T (dP^T scale + nd) -> bf16, into TMEM (aliasing dP^T,
 //                for MMA4) and 128B-swizzled into SMEM (for MMA5); and, as TMEM
 //                lane r of dQ^T, stages head-dim column r of its 64 dQ rows.
 //              At the end warpgroup 0 writes dV and warpgroup 1 writes dK.
@@ -80,14 +82,15 @@ struct BwdPreParams {
   const __nv_bfloat16* dO;  // [BH, N, D]
   const float* lse;         // [BH, N]
   float* dq;                // [BH, N, D], zeroed here
-  float* lse2;              // workspace [BH, Np]
-  float* dd;                // workspace [BH, Np]
+  float* nl;                // workspace [BH, Np]: -lse log2(e)
+  float* nd;                // workspace [BH, Np]: -D scale
   int BH, N, Np;
+  float scale;
 };
 
-// One warp per row: D = sum_c dO_c O_c (f32), lse2 = lse * log2(e) (+inf where
-// lse = -inf or the row is padding), dq row = 0.  Grid: BH * Np / 64 blocks of
-// 256 threads, 8 rows per warp.
+// One warp per row: D = sum_c dO_c O_c (f32); nl = -lse log2(e) (-inf where
+// lse = -inf or the row is padding); nd = -D scale; dq row = 0.  Grid: BH * Np / 64
+// blocks of 256 threads, 8 rows per warp.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p) {
   constexpr int EPL = D / 32;  // elements per lane
@@ -100,8 +103,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
     const size_t ws = static_cast<size_t>(bh) * p.Np + row;
     if (row >= p.N) {
       if (lane == 0) {
-        p.lse2[ws] = INFINITY;
-        p.dd[ws] = 0.f;
+        p.nl[ws] = -INFINITY;
+        p.nd[ws] = 0.f;
       }
       continue;
     }
@@ -130,8 +133,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
       const float l = p.lse[static_cast<size_t>(bh) * p.N + row];
-      p.lse2[ws] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-      p.dd[ws] = acc;
+      p.nl[ws] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+      p.nd[ws] = -acc * p.scale;
     }
   }
 }
@@ -140,8 +143,8 @@ struct BwdParams {
   float* dq;                // [BH, N, D], accumulated by tiled reduce-adds (tensor map tm_dq)
   float* dk;                // [BH, N, D]
   float* dv;                // [BH, N, D]
-  const float* lse2;        // [BH, Np]
-  const float* dd;          // [BH, Np]
+  const float* nl;          // [BH, Np]: -lse log2(e)
+  const float* nd;          // [BH, Np]: -D scale
   const int* kv_len;        // [B] or null
   int BH, H, N, Np;
   int n_kt;                 // key tiles per head
@@ -165,7 +168,7 @@ struct BwdLayout {
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
   static constexpr int OFF_DS = OFF_DO + STAGES * TILE;  // dS^T: 2 column blocks of 64 queries
-  static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: lse2[128], D[128]
+  static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: nl[128], nd[128]
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
   // barriers: kv_full, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full, dp_full,
   //           ds_full, dq_full, dq_empty, red_ready[2], ds_free, dkv_done, drain
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = kv_full + 1;         // [S] Q_t and its lse2 / D rows have landed
+  uint64_t* q_full = kv_full + 1;         // [S] Q_t and its nl / nd rows have landed
   uint64_t* do_full = q_full + STAGES;    // [S] dO_t has landed
   uint64_t* q_empty = do_full + STAGES;   // [S] MMA4_t, the last reader of Q_t, is done
   uint64_t* do_empty = q_empty + STAGES;  // [S] the dQ_t half staged in dO_t's buffer has been read
@@ -290,10 +293,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
           tma_load_3d(smem + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, &q_full[st], kb * 64, q0, bh);
-        // lse2 and D of the tile's 128 queries (rows padded to a multiple of 128)
+        // nl and nd of the tile's 128 queries (rows padded to a multiple of 128)
         const size_t ws = static_cast<size_t>(bh) * p.Np + q0;
-        bulk_load(smem + L::OFF_STAT + st * 1024, p.lse2 + ws, 512, &q_full[st]);
-        bulk_load(smem + L::OFF_STAT + st * 1024 + 512, p.dd + ws, 512, &q_full[st]);
+        bulk_load(smem + L::OFF_STAT + st * 1024, p.nl + ws, 512, &q_full[st]);
+        bulk_load(smem + L::OFF_STAT + st * 1024 + 512, p.nd + ws, 512, &q_full[st]);
         *issued_q = t + 1;
         if (t >= STAGES && !mbar_wait(&do_empty[st], eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
         mbar_arrive_expect_tx(&do_full[st], L::TILE);
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(384, 1)
     const bool key_ok = (k0 + r) < kv_limit;
     const float sl = p.scale_log2, scale = p.scale;
     const uint32_t ds_row = smem_u32(smem + L::OFF_DS) + h * L::COLBLK + r * 128;
-    const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + stage * 1024: lse2; + 512: D
+    const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + stage * 1024: nl; + 512: nd
     bool ok = true;
     float pr[64];
     // Pass t forms P^T and dS^T of tile u = t + 1 around the drain of dQ^T_t:
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(384, 1)
       const int qu = (i0 + u) * L::BM + h * 64;  // first query of this half of tile u
       if (u < n_it) {
         // q_full is already complete here (S^T_u exists); waiting on it makes the
-        // stage's lse2 / D rows visible to these threads
+        // stage's nl / nd rows visible to these threads
         if (!__all_sync(0xffffffffu, mbar_wait(s_full, u & 1, wc, ST_BWD_TIMEOUT_S) &&
                                          mbar_wait(&q_full[su], (u / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
           ok = false;
@@ -452,22 +455,33 @@ __global__ void __launch_bounds__(384, 1)
         // causal: key k0 + r is visible to query qu + j iff j >= r - (qu - k0),
         // one later in the strict mode (a query does not see its own key)
         const int jmin = p.causal ? r - (qu - k0) + (p.causal == 2 ? 1 : 0) : -1;
-        const uint32_t lse2_s = stat + su * 1024;
+        // only tiles on the diagonal or past a key-padding edge mask anything
+        const bool masked = __any_sync(0xffffffffu, !key_ok || jmin > 0);
+        const uint32_t nl_s = stat + su * 1024;
+        const uint64_t sl2 = f2_pack(sl, sl);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t sr[32];
           FA_TMEM_LD32(s_col + half * 32, sr);
           tmem_wait_ld();
           FA_REG_FENCE32(sr);
+          if (masked) {
+#pragma unroll
+            for (int w = 0; w < 32; ++w)
+              if (!key_ok || half * 32 + w < jmin) sr[w] = __float_as_uint(-INFINITY);
+          }
 #pragma unroll
           for (int j4 = 0; j4 < 32; j4 += 4) {
-            float lv[4];
-            ld_shared_v4f(lse2_s + (half * 32 + j4) * 4, lv);
+            float nl[4];
+            ld_shared_v4f(nl_s + (half * 32 + j4) * 4, nl);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const int j = half * 32 + j4 + w;
-              const float e = ex2_approx(fmaf(__uint_as_float(sr[j4 + w]), sl, -lv[w]));
-              pr[j] = (key_ok && j >= jmin) ? e : 0.f;
+            for (int w = 0; w < 4; w += 2) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
+                               f2_pack(nl[w], nl[w + 1])),
+                        x0, x1);
+              pr[half * 32 + j4 + w] = ex2_approx(x0);
+              pr[half * 32 + j4 + w + 1] = ex2_approx(x1);
             }
           }
         }
@@ -517,7 +531,8 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t dd_s = stat + su * 1024 + 512;
+        const uint32_t nd_s = stat + su * 1024 + 512;
+        const uint64_t sc2 = f2_pack(scale, scale);
         uint32_t dsk[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -528,13 +543,19 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int j4 = 0; j4 < 32; j4 += 4) {
             const int j = half * 32 + j4;
-            float dv4[4];
-            ld_shared_v4f(dd_s + j * 4, dv4);
-            float g[4];
+            float nd[4];
+            ld_shared_v4f(nd_s + j * 4, nd);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) g[w] = pr[j + w] * (__uint_as_float(dpr[j4 + w]) - dv4[w]) * scale;
-            dsk[j / 2] = pack_bf16x2(g[0], g[1]);
-            dsk[j / 2 + 1] = pack_bf16x2(g[2], g[3]);
+            for (int w = 0; w < 4; w += 2) {
+              // dS = P (dP scale - D scale)
+              const uint64_t g =
+                  f2_mul(f2_fma(f2_pack(__uint_as_float(dpr[j4 + w]), __uint_as_float(dpr[j4 + w + 1])), sc2,
+                                f2_pack(nd[w], nd[w + 1])),
+                         f2_pack(pr[j + w], pr[j + w + 1]));
+              float g0, g1;
+              f2_unpack(g, g0, g1);
+              dsk[(j + w) / 2] = pack_bf16x2(g0, g1);
+            }
           }
         }
         // The dS buffer is free once the dQ^T_t half staged there has been read.

@@ -238,11 +238,12 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   pp.dO = static_cast<const __nv_bfloat16*>(dO);
   pp.lse = lse;
   pp.dq = dq;
-  pp.lse2 = ws;
-  pp.dd = ws + static_cast<size_t>(BH) * Np;
+  pp.nl = ws;
+  pp.nd = ws + static_cast<size_t>(BH) * Np;
   pp.BH = BH;
   pp.N = N;
   pp.Np = static_cast<int>(Np);
+  pp.scale = scale;
   fa::bwd_preprocess_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch bwd_preprocess_kernel");
@@ -258,8 +259,8 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.lse2 = pp.lse2;
-  p.dd = pp.dd;
+  p.nl = pp.nl;
+  p.nd = pp.nd;
   p.kv_len = kv_len;
   p.BH = BH;
   p.H = H;
