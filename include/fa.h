@@ -97,7 +97,8 @@ fa_status fa_fwd_qk(int dtype, const void* q, const void* k, const void* v, void
 /*
  * fa_bwd_workspace_size -- bytes of device workspace fa_bwd / fa_bwd_ex need for
  * this problem: two float32 arrays of B*H*Np entries, Np = N rounded up to a
- * multiple of 128 (per-row D = rowsum(dO * O) and lse * log2(e)).  Returns 0 for
+ * multiple of 128 (per query row: -lse * log2(e), and -scale * D with
+ * D = rowsum(dO * O)).  The content is private to the call.  Returns 0 for
  * non-positive sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
