@@ -216,18 +216,21 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool = False, kv_len=None):
         D_i = sum_j P_ij dP_ij,   dS = P * (dP - D),
         dQ = scale * dS K,         dK = scale * dS^T Q.
 
-    A fully masked row has P = 0 and contributes nothing.
+    A fully masked row has P = 0 and contributes nothing.  q and do may have a
+    different length Nq from k and v (Nk); the mask is then visible_mask's
+    (queries are the last Nq positions of the key sequence), as in the forward.
     Returns (dQ, dK, dV) float64 with the shapes of (q, k, v).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
-    B, H, N, _ = q.shape
+    B, H, Nq, _ = q.shape
+    Nk = k.shape[2]
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     scale = float(scale)
     for b in range(B):
         kl = None if kv_len is None else int(kv_len[b])
         for h in range(H):
             s = score_matrix(q[b, h], k[b, h], scale)
-            s = apply_mask(s, visible_mask(N, N, causal, kl))
+            s = apply_mask(s, visible_mask(Nq, Nk, causal, kl))
             m = row_max(s)
             e = shifted_exp(s, m)
             l = e.sum(axis=-1)
