@@ -95,9 +95,9 @@ fa_status fa_fwd_qk(int dtype, const void* q, const void* k, const void* v, void
                     void* stream);
 
 /*
- * fa_bwd_workspace_size -- bytes of device workspace fa_bwd / fa_bwd_ex need for
- * this problem: two float32 arrays of B*H*Np entries, Np = N rounded up to a
- * multiple of 128 (per query row: -lse * log2(e), and -scale * D with
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd / fa_bwd_ex /
+ * fa_bwd_qk need for this problem (N = the number of query rows): two float32
+ * arrays of B*H*Np entries, Np = N rounded up to a multiple of 128 (per query row: -lse * log2(e), and -scale * D with
  * D = rowsum(dO * O)).  The content is private to the call.  Returns 0 for
  * non-positive sizes.
  */
@@ -134,6 +134,23 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
                     int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_bwd_qk -- as fa_bwd_ex, for the forward fa_fwd_qk: Nq queries and Nk keys
+ * per head, the queries read as the last Nq positions of the key sequence, so a
+ * causal mask is aligned bottom-right (query i sees keys j <= i + Nk - Nq, or
+ * j < i + Nk - Nq when strict).  The pages treat Nq = Nk only; this is the
+ * reading fa_fwd_qk documents.
+ *   q, o, dO       : [B, H, Nq, d];  lse : [B, H, Nq];  dq : [B, H, Nq, d]
+ *   k, v           : [B, H, Nk, d];  dk, dv : [B, H, Nk, d]
+ *   kv_len         : NULL or a device pointer to B int32 values, clamped to [0, Nk]
+ *   workspace      : at least fa_bwd_workspace_size(B, H, Nq, d) bytes
+ * Query rows that see no key get dq = 0; keys no query sees get dk = dv = 0.
+ * Errors as fa_bwd_ex; Nk < 1 is FA_ERR_INVALID.
+ */
+fa_status fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                    int B, int H, int Nq, int Nk, int d, float scale, int causal, void* stream);
 
 /*
  * fa_merge -- combine partial attention results computed over disjoint key

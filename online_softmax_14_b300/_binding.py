@@ -53,6 +53,8 @@ _lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _
 _lib.fa_bwd.restype = _i
 _lib.fa_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_bwd_ex.restype = _i
+_lib.fa_bwd_qk.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_bwd_qk.restype = _i
 _lib.fa_merge.argtypes = [_i, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.fa_merge.restype = _i
 _lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
@@ -220,24 +222,38 @@ def attention_fwd(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
     return o, lse
 
 
+def fa_bwd_qk(q, k, v, o, do, lse, kv_len, dq, dk, dv, workspace, workspace_bytes, B, H, Nq, Nk, d, scale, causal,
+              stream=None) -> None:
+    _check(_lib.fa_bwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(kv_len), _ptr(dq),
+                          _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, Nq, Nk, d, float(scale),
+                          _causal(causal), _stream(stream)))
+
+
 def attention_bwd(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, stream=None):
-    """dQ, dK, dV (float32) of attention over bf16 [B, H, N, d] CUDA tensors.
+    """dQ, dK, dV (float32) of attention over bf16 CUDA tensors: q, o, do
+    [B, H, Nq, d] and k, v [B, H, Nk, d] (Nq may differ from Nk; a causal mask is
+    then aligned bottom-right, as in ``attention_fwd``).
 
     ``o`` and ``lse`` are the forward's outputs for the same inputs.  Allocates
-    the gradients and the workspace with PyTorch, then runs ``fa_bwd_ex``.
+    the gradients and the workspace with PyTorch, then runs ``fa_bwd_qk``.
     """
-    for t in (q, k, v, o, do):
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16 and t.shape == q.shape):
-            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors of shape [B, H, N, d]")
-    B, H, N, d = q.shape
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    for t, shape in ((q, q.shape), (o, q.shape), (do, q.shape), (k, (B, H, Nk, d)), (v, (B, H, Nk, d))):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16 and tuple(t.shape) == tuple(shape)):
+            raise ValueError("q, o, do must be contiguous bf16 CUDA tensors of shape [B, H, Nq, d] and k, v of "
+                             "shape [B, H, Nk, d]")
     if scale is None:
         scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-    dk = torch.empty_like(dq)
-    dv = torch.empty_like(dq)
-    ws_bytes = fa_bwd_workspace_size(B, H, N, d)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty_like(dk)
+    ws_bytes = fa_bwd_workspace_size(B, H, Nq, d)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     if kv_len is not None:
         kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
-    fa_bwd_ex(q, k, v, o, do, lse.contiguous(), kv_len, dq, dk, dv, ws, ws_bytes, B, H, N, d, scale, causal, stream)
+    fa_bwd_qk(q, k, v, o, do, lse.contiguous(), kv_len, dq, dk, dv, ws, ws_bytes, B, H, Nq, Nk, d, scale, causal,
+              stream)
     return dq, dk, dv

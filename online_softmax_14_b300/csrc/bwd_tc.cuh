@@ -141,16 +141,18 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
 
 struct BwdParams {
   float* dq;                // [BH, N, D], accumulated by tiled reduce-adds (tensor map tm_dq)
-  float* dk;                // [BH, N, D]
-  float* dv;                // [BH, N, D]
+  float* dk;                // [BH, Nk, D]
+  float* dv;                // [BH, Nk, D]
   const float* nl;          // [BH, Np]: -lse log2(e)
   const float* nd;          // [BH, Np]: -D scale
   const int* kv_len;        // [B] or null
-  int BH, H, N, Np;
+  int BH, H, N, Np;         // N queries per head
+  int Nk;                   // keys per head
   int n_kt;                 // key tiles per head
   float scale;              // score multiplier
   float scale_log2;         // scale * log2(e)
-  int causal;               // 0 none, 1 key k visible iff k <= row, 2 iff k < row
+  int causal;               // 0 none, else key k visible to query row i iff k < i + qoff
+  int qoff;                 // (Nk - N) + 1 (causal 1) or (Nk - N) (causal 2, strict)
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -227,11 +229,13 @@ __global__ void __launch_bounds__(384, 1)
   const int kt = static_cast<int>(blockIdx.x) % p.n_kt;
   const int b = bh / p.H;
   const int k0 = kt * L::BN;
-  int kv_limit = p.N;
-  if (p.kv_len) kv_limit = min(p.N, max(0, p.kv_len[b]));
+  int kv_limit = p.Nk;
+  if (p.kv_len) kv_limit = min(p.Nk, max(0, p.kv_len[b]));
   const int n_qt = (p.N + L::BM - 1) / L::BM;
-  const int i0 = p.causal ? k0 / L::BM : 0;  // first query tile that sees a key of this tile
-  const int n_it = (k0 < kv_limit) ? n_qt - i0 : 0;
+  // first query tile that sees a key of this tile: causal, key k0 is visible to
+  // query rows i >= k0 - qoff + 1
+  const int i0 = p.causal ? max(0, k0 - p.qoff + 1) / L::BM : 0;
+  const int n_it = (k0 < kv_limit && i0 < n_qt) ? n_qt - i0 : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -432,6 +436,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_col = lane_base + L::TM_S + h * 64;   // this half's S^T, then its P^T
     const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T, then dQ^T
     const bool key_ok = (k0 + r) < kv_limit;
+    const int jrow = k0 + r - p.qoff + 1;  // causal: first visible query row of key k0 + r
     const float sl = p.scale_log2, scale = p.scale;
     const uint32_t ds_row = smem_u32(smem + L::OFF_DS) + h * L::COLBLK + r * 128;
     const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + stage * 1024: nl; + 512: nd
@@ -452,9 +457,8 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        // causal: key k0 + r is visible to query qu + j iff j >= r - (qu - k0),
-        // one later in the strict mode (a query does not see its own key)
-        const int jmin = p.causal ? r - (qu - k0) + (p.causal == 2 ? 1 : 0) : -1;
+        // causal: key k0 + r is visible to query qu + j iff k0 + r < qu + j + qoff
+        const int jmin = p.causal ? jrow - qu : -1;
         // only tiles on the diagonal or past a key-padding edge mask anything
         const bool masked = __any_sync(0xffffffffu, !key_ok || jmin > 0);
         const uint32_t nl_s = stat + su * 1024;
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(384, 1)
     if (ok) {
       tc_fence_after();
       const int key = k0 + r;
-      float* out = (h == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.N + key) * D;
+      float* out = (h == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D;
       const uint32_t col = lane_base + (h == 0 ? L::TM_DV : L::TM_DK);
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (key < p.N) {
+        if (key < p.Nk) {
           float4* o4 = reinterpret_cast<float4*>(out + cb * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)

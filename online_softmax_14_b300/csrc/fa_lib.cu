@@ -222,14 +222,14 @@ size_t bwd_ws_bytes(int B, int H, int N) {
 }
 
 fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                     const int32_t* kv_len, float* dq, float* dk, float* dv, float* ws, int B, int H, int N,
+                     const int32_t* kv_len, float* dq, float* dk, float* dv, float* ws, int B, int H, int N, int Nk,
                      float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
   constexpr int D = 128;
   using L = fa::BwdLayout<kStagesBwd>;
   const int BH = B * H;
   const long long Np = bwd_np(N);
   const long long pre_blocks = static_cast<long long>(BH) * (Np / 64);
-  const long long n_kt = (N + L::BN - 1) / L::BN;
+  const long long n_kt = (Nk + L::BN - 1) / L::BN;
   const long long blocks = n_kt * BH;
   if (pre_blocks > 0x7fffffffll || blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
 
@@ -251,8 +251,8 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   CUtensorMap mq, mk, mv, mdo, mdq;
   fa_status s;
   if ((s = make_map(&mq, q, D, N, BH, "q", 128)) != FA_OK) return s;
-  if ((s = make_map(&mk, k, D, N, BH, "k", 128)) != FA_OK) return s;
-  if ((s = make_map(&mv, v, D, N, BH, "v", 128)) != FA_OK) return s;
+  if ((s = make_map(&mk, k, D, Nk, BH, "k", 128)) != FA_OK) return s;
+  if ((s = make_map(&mv, v, D, Nk, BH, "v", 128)) != FA_OK) return s;
   if ((s = make_map(&mdo, dO, D, N, BH, "dO", 128)) != FA_OK) return s;
   if ((s = make_map_f32(&mdq, dq, D, N, BH, "dq", 64)) != FA_OK) return s;
   fa::BwdParams p{};
@@ -266,10 +266,12 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.H = H;
   p.N = N;
   p.Np = static_cast<int>(Np);
+  p.Nk = Nk;
   p.n_kt = static_cast<int>(n_kt);
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal = causal;
+  p.qoff = causal_qoff(N, Nk, causal);
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
@@ -343,26 +345,35 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return bwd_ws_bytes(B, H, N);
 }
 
-fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+fa_status fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
-                    int B, int H, int N, int d, float scale, int causal, void* stream) {
+                    int B, int H, int Nq, int Nk, int d, float scale, int causal, void* stream) {
   t_err[0] = '\0';
   fa_status s;
   if ((s = check_causal(causal)) != FA_OK) return s;
-  if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
+  if (Nk < 1) return fail(FA_ERR_INVALID, "Nk must be >= 1 (got %d)", Nk);
+  if (static_cast<long long>(Nk) * d > (1ll << 38)) return fail(FA_ERR_UNSUPPORTED, "problem too large (Nk*d)");
+  if ((s = check_common(q, k, v, o, lse, B, H, Nq, d, scale, 16)) != FA_OK) return s;
   if (!dO || !lse || !dq || !dk || !dv || !workspace)
     return fail(FA_ERR_INVALID, "dO, lse, dq, dk, dv and workspace must be non-null device pointers");
   if (!aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 16))
     return fail(FA_ERR_INVALID, "dO, dq, dk, dv and workspace must be 16-byte aligned");
   if (d != 128) return fail(FA_ERR_UNSUPPORTED, "bf16 backward serves d = 128 (got %d)", d);
-  const size_t need = bwd_ws_bytes(B, H, N);
+  const size_t need = bwd_ws_bytes(B, H, Nq);
   if (workspace_bytes < need)
     return fail(FA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes,
                 need);
   DeviceState* ds = nullptr;
   if ((s = device_state(&ds)) != FA_OK) return s;
-  return launch_bwd(q, k, v, o, dO, lse, kv_len, dq, dk, dv, static_cast<float*>(workspace), B, H, N, scale, causal,
-                    static_cast<cudaStream_t>(stream), *ds);
+  return launch_bwd(q, k, v, o, dO, lse, kv_len, dq, dk, dv, static_cast<float*>(workspace), B, H, Nq, Nk, scale,
+                    causal, static_cast<cudaStream_t>(stream), *ds);
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    const int32_t* kv_len, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                    int B, int H, int N, int d, float scale, int causal, void* stream) {
+  return fa_bwd_qk(q, k, v, o, dO, lse, kv_len, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, scale, causal,
+                   stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
@@ -540,6 +551,6 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if ((s = device_state(&ds)) != FA_OK) return s;
   float* ws = nullptr;
   if ((s = noalloc_scratch(&ws)) != FA_OK) return s;
-  return launch_bwd(q, k, v, o, dO, lse, nullptr, dq, dk, dv, ws, B, H, N, scale, causal,
+  return launch_bwd(q, k, v, o, dO, lse, nullptr, dq, dk, dv, ws, B, H, N, N, scale, causal,
                     static_cast<cudaStream_t>(stream), *ds);
 }

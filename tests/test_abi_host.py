@@ -127,6 +127,26 @@ def test_bwd_host_validation(kw, status):
     assert fa.fa_last_error_string() != ""
 
 
+def _bwd_qk(q=P, k=P, v=P, o=P, do=P, lse=P, kv=None, dq=P, dk=P, dv=P, ws=P, ws_bytes=1 << 20, Bs=1, H=1, Nq=16,
+            Nk=48, d=128, scale=0.125, causal=1):
+    return B.fa_status_raw("fa_bwd_qk", q, k, v, o, do, lse, kv, dq, dk, dv, ws, ctypes.c_size_t(ws_bytes), Bs, H,
+                           Nq, Nk, d, ctypes.c_float(scale), causal, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Nk=0), B.FA_ERR_INVALID),
+    (dict(Nq=0), B.FA_ERR_INVALID),
+    (dict(do=None), B.FA_ERR_INVALID),
+    (dict(dv=P + 4), B.FA_ERR_INVALID),
+    (dict(ws_bytes=16), B.FA_ERR_INVALID),      # smaller than fa_bwd_workspace_size(B, H, Nq, d)
+    (dict(d=64), B.FA_ERR_UNSUPPORTED),
+    (dict(causal=3), B.FA_ERR_INVALID),
+])
+def test_bwd_qk_host_validation(kw, status):
+    assert _bwd_qk(**kw) == status
+    assert fa.fa_last_error_string() != ""
+
+
 def _merge(dtype=0, op=P, lp=P, n=2, o=P, lse=None, Bs=1, H=1, N=16, d=64):
     return B.fa_status_raw("fa_merge", dtype, op, lp, n, o, lse, Bs, H, N, d, None)
 
