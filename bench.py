@@ -51,10 +51,10 @@ L2_BYTES = 126 * 1024 * 1024
 # DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture,
 # valid only for the forward kernel sources whose digest is recorded with it.
 # The N=8192 launch was not captured itself: B=2 H=32 N=4096 (same kernel, half
-# the units) read 201,408,768 and wrote 49,077,504 bytes, and the traffic scales
+# the units) read 201,429,248 and wrote 49,031,680 bytes, and the traffic scales
 # with B*H*N*d (Q, K, V read once, O written once; K/V re-reads hit L2).
-NCU_TRAFFIC = {"bf16_causal_B2_H32_N8192_d128": {"bytes": 2 * (201408768 + 49077504),
-                                                 "src_digest": "f627616c5fe8af62",
+NCU_TRAFFIC = {"bf16_causal_B2_H32_N8192_d128": {"bytes": 2 * (201429248 + 49031680),
+                                                 "src_digest": "ad9074c152faa792",
                                                  "how": "scaled x2 from an ncu capture of B=2 H=32 N=4096"}}
 FWD_SOURCES = ("fwd_tc.cuh", "ptx.cuh", "fa_lib.cu")
 

@@ -212,7 +212,8 @@ const char* fa_last_error_string(void);
  * fa_check_device_error -- synchronise `stream`, then read and clear the
  * library's device status word on the current device.  Returns FA_ERR_TIMEOUT
  * if any kernel since the last check gave up on a pipeline wait, FA_ERR_CUDA if
- * the stream reported an error, else FA_OK.
+ * the stream reported an error or a kernel found its shared memory misaligned
+ * (it then did nothing), else FA_OK.
  */
 fa_status fa_check_device_error(void* stream);
 

@@ -469,6 +469,9 @@ fa_status fa_check_device_error(void* stream) {
   if (word == 0) return FA_OK;
   if ((e = cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "clear status word");
+  if (word & fa::ST_BWD_SMEM_ALIGN)
+    return fail(FA_ERR_CUDA, "backward kernel found its shared memory base misaligned and did nothing (status bits "
+                "0x%x)", word);
   return fail(FA_ERR_TIMEOUT, "kernel pipeline wait timed out (status bits 0x%x)", word);
 }
 
