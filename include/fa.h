@@ -29,6 +29,11 @@
  *   - Every kernel waits on its pipeline with a time limit; a wait that runs out
  *     ends the kernel early with garbage outputs and records FA_ERR_TIMEOUT, so
  *     a broken pipeline cannot hang the GPU.
+ *   - Per device, the library keeps the device addresses of its own variables
+ *     and the kernels' shared-memory limits.  It sets them up on the first call
+ *     in each CUDA context and again whenever the current context has changed
+ *     (for instance after the caller ran cudaDeviceReset), so such a reset is
+ *     safe between calls; it is not safe while the library's work is in flight.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -189,8 +194,10 @@ fa_status fa_merge(int dtype, const void* o_parts, const float* lse_parts, int n
  *   Limit: B * H * Np <= FA_BWD_NOALLOC_MAX_ROWS, where Np is N rounded up to
  *   a multiple of 128.  Larger problems return FA_ERR_UNSUPPORTED with a message
  *   naming the limit; use fa_bwd with a workspace for them.
- *   The first call on each device looks up the array's device address with
- *   cudaGetSymbolAddress, so make that first call before any stream capture.
+ *   The first call on each device (and the first after the CUDA context has
+ *   changed, e.g. after a cudaDeviceReset) looks up the array's device address
+ *   with cudaGetSymbolAddress, so make that first call before any stream
+ *   capture.
  *   All calls share the one array.  Calls whose work overlaps on the GPU (say,
  *   on two streams without ordering) corrupt each other's gradients; order
  *   them.  Stale contents left by an earlier call are harmless: every part of
@@ -209,11 +216,13 @@ const char* fa_status_string(int status);
 const char* fa_last_error_string(void);
 
 /*
- * fa_check_device_error -- synchronise `stream`, then read and clear the
- * library's device status word on the current device.  Returns FA_ERR_TIMEOUT
- * if any kernel since the last check gave up on a pipeline wait, FA_ERR_CUDA if
- * the stream reported an error or a kernel found its shared memory misaligned
- * (it then did nothing), else FA_OK.
+ * fa_check_device_error -- synchronise `stream`, then take the library's device
+ * status word on the current device (read and cleared in one atomic exchange,
+ * enqueued on `stream`, so a bit set meanwhile by a kernel on another stream is
+ * reported by a later call, never lost).  Returns FA_ERR_TIMEOUT if any kernel
+ * since the last check gave up on a pipeline wait, FA_ERR_CUDA if the stream
+ * reported an error or a kernel found its shared memory misaligned (it then did
+ * nothing), else FA_OK.
  */
 fa_status fa_check_device_error(void* stream);
 
@@ -225,9 +234,12 @@ void fa_set_wait_timeout_ms(int ms);
 
 /*
  * fa_debug_inject -- test hook.  code 1 makes the next fa_fwd bf16 launches'
- * producers stop feeding K/V tiles after the first one, so that the consumers'
- * bounded waits run out and the launch reports FA_ERR_TIMEOUT.  code 0 (the
- * default) turns it off.  Nothing faults, traps or hangs either way.
+ * producers stop feeding K/V tiles after the first one; code 2 makes the next
+ * fa_bwd launches' producers stop feeding Q/dO tiles after the first one.
+ * Either way the consumers' bounded waits run out, each CTA drains the copies
+ * and tensor-core work it has in flight, frees its tensor memory and exits, and
+ * fa_check_device_error reports FA_ERR_TIMEOUT.  code 0 (the default) turns it
+ * off.  Nothing faults, traps or hangs either way.
  */
 void fa_debug_inject(int code);
 

@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import glob
 import os
+import re
 import subprocess
 import sys
 
@@ -41,6 +42,20 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
+def spilling_kernels(ptxas_log: str) -> list:
+    """Kernels for which ptxas -v reports spill stores or loads, with the line."""
+    out, kernel = [], None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            kernel = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and (int(m.group(1)) or int(m.group(2))):
+            out.append(f"{kernel}: {line.strip()}")
+    return out
+
+
 def build_library(force: bool = False, verbose: bool = False) -> str:
     """Compile libfa.so if it is missing or older than a source; return its path."""
     if not force and not is_stale():
@@ -51,10 +66,9 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
     log = r.stdout + r.stderr
-    if "spill stores" in log:
-        for line in log.splitlines():
-            if "spill" in line and not line.strip().startswith("0 bytes stack frame, 0 bytes spill stores"):
-                print("warning:", line.strip(), file=sys.stderr)
+    spills = spilling_kernels(log)
+    if spills:
+        raise RuntimeError("register spills (every kernel must report 0 bytes):\n" + "\n".join(spills))
     if verbose:
         print(" ".join(cmd))
         print(log)

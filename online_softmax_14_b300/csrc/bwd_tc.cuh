@@ -25,14 +25,21 @@
 //       MMA3  dV    += P^T_t dO_t          (A = P^T from TMEM, B = dO_t MN-major)
 //       MMA4  dK    += dS^T_t Q_t          (A = dS^T from TMEM, B = Q_t MN-major)
 //       MMA5  dQ^T_t = K^T dS_t            (A = K MN-major, B = dS^T MN-major, SMEM)
-//    issued as MMA3_t, MMA1_{t+1}, MMA4_t, MMA5_t, MMA2_{t+1}: S^T of the next
-//    tile is ready while tile t finishes, and dK / dQ of tile t run while the
-//    elementwise warps form P^T_{t+1}.  dS carries the factor `scale`, so dK and
-//    dQ need no further scaling.
-//    dQ^T_t is staged row-major in shared memory (the dO_t buffer and the dS
-//    buffer, both free once MMA5_t has run) and added into global dQ with two
-//    tiled TMA reduce-adds (cp.reduce.async.bulk.tensor .add.f32), which skip
-//    the rows past N.
+//    issued as MMA3_t, MMA4_t, MMA5_t, MMA1_{t+1}, MMA2_{t+1}.  dS carries the
+//    factor `scale`, so dK and dQ need no further scaling.
+//    dQ^T_t is staged row-major in shared memory -- the query half 0-63 in dO_t's
+//    buffer, the half 64-127 in Q_t's buffer -- and added into global dQ with two
+//    tiled TMA reduce-adds (cp.reduce.async.bulk.tensor .add.f32), which skip the
+//    rows past N.  The producer refills those buffers only after the reduce-adds
+//    have read them.
+//    Why this order: the staging needs 64 KB of shared memory that is free for
+//    as long as a reduce-add reads it (about as long as two products take), and
+//    only the tile's own Q and dO buffers qualify -- provided S^T_{t+1} = K
+//    Q_{t+1}^T is not issued early (then Q_{t+2} would be needed before the
+//    reduce-add has released Q_t's buffer).  The dS buffer, which MMA5_t reads,
+//    is thus never used for staging, and the next tile's dS^T is not held up by
+//    a reduce-add.  While the elementwise warps form P^T_{t+1}, the tensor cores
+//    run MMA2_{t+1}; while they form dS^T_{t+1}, MMA3_{t+1}.
 //
 // Roles (384 threads):
 //   warp 0     TMA producer: K, V once; then Q_t + nl_t + nd_t and dO_t into the
@@ -40,25 +47,33 @@
 //   warp 1     MMA issuer (lane 0 of the converged warp) and tensor-memory owner.
 //   warp 2     dQ reducer: issues the reduce-adds once a half is staged and
 //              hands the buffers back when the copies have read them.
+//   warp 3     no role.
 //   warps 4-7  elementwise warpgroup 0, query columns 0-63 of every tile;
 //   warps 8-11 elementwise warpgroup 1, query columns 64-127.
 //              Thread r owns key row r (TMEM lane r) of S^T and dP^T:
 //                P^T = 2^(S^T scale log2e + nl) with the causal / padding mask,
 //                written back to TMEM as bf16 (aliasing S^T); then
-//                dS^T = P^T (dP^T scale + nd) -> bf16, into TMEM (aliasing dP^T,
-//                for MMA4) and 128B-swizzled into SMEM (for MMA5); and, as TMEM
-//                lane r of dQ^T, stages head-dim column r of its 64 dQ rows.
+//                dS^T = P^T (dP^T scale + nd) -> bf16, into TMEM (aliasing
+//                dP^T, for MMA4) and 128B-swizzled into SMEM (for MMA5); and, as
+//                TMEM lane r of dQ^T, stages head-dim column r of its 64 dQ rows.
 //              At the end warpgroup 0 writes dV and warpgroup 1 writes dK.
 //
 // Tensor memory (512 columns, f32 unless noted):
 //   [0,128)   S^T_t, then P^T_t (bf16: queries 0-63 in [0,32), 64-127 in [64,96))
-//   [128,256) dP^T_t, then dS^T_t (bf16, same layout as P^T), then dQ^T_t
+//   [128,256) dP^T_t, then dS^T_t (bf16, laid out like P^T), then dQ^T_t
 //   [256,384) dV   [384,512) dK
 //
 // Every wait is bounded, as in the forward kernel: a wait that runs out records
 // a status bit, the CTA drains what it has in flight and exits.
 #pragma once
+#include "exp2_poly.cuh"
 #include "ptx.cuh"
+
+// Every FA_BWD_EXP2_FMA_EVERY-th pair of probabilities takes its exponentials on
+// the FMA pipe (exp2_fma2) instead of the special-function unit; 0 = none.
+#ifndef FA_BWD_EXP2_FMA_EVERY
+#define FA_BWD_EXP2_FMA_EVERY 0
+#endif
 
 namespace fa {
 
@@ -76,6 +91,11 @@ enum : unsigned {
   ST_BWD_TIMEOUT_RED = 1u << 18,
   ST_BWD_SMEM_ALIGN = 1u << 19,   // dynamic shared memory base not aligned enough (kernel did nothing)
 };
+
+// Register shares (launch: 384 threads x 168): warps 0-3 (producer, MMA issuer,
+// reducer, idle) keep BWD_REGS_LOW, the elementwise warpgroups get BWD_REGS_HIGH.
+constexpr uint32_t BWD_REGS_LOW = 56, BWD_REGS_HIGH = 216;
+static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= 384 * 168, "register split exceeds the launch");
 
 struct BwdPreParams {
   const __nv_bfloat16* o;   // [BH, N, D]
@@ -155,7 +175,9 @@ struct BwdParams {
   int qoff;                 // (Nk - N) + 1 (causal 1) or (Nk - N) (causal 2, strict)
   unsigned* status;
   unsigned long long timeout_ns;
+  int inject;               // test hook: 2 = producer stops after the first Q / dO tile
 };
+
 
 template <int STAGES>
 struct BwdLayout {
@@ -173,8 +195,8 @@ struct BwdLayout {
   static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: nl[128], nd[128]
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
   // barriers: kv_full, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full, dp_full,
-  //           ds_full, dq_full, dq_empty, red_ready[2], ds_free, dkv_done, drain
-  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 2 + 3;
+  //           ds_full, dq_full, dq_empty, red_ready[2], dkv_done, drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int BYTES = 232448;             // the whole per-CTA budget
@@ -183,6 +205,58 @@ struct BwdLayout {
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
   static_assert(SLACK >= 0, "shared memory budget");
 };
+
+// Shared-memory addresses (32-bit) of the backward kernel's buffers and
+// barriers, from the 1024-aligned base of its dynamic shared memory.
+template <int STAGES>
+struct BwdSmem {
+  using L = BwdLayout<STAGES>;
+  uint32_t base;
+  __device__ __forceinline__ explicit BwdSmem(uint32_t raw) : base((raw + 1023u) & ~1023u) {}
+  __device__ __forceinline__ uint32_t bar(int i) const { return base + L::OFF_BAR + 8 * i; }
+  __device__ __forceinline__ uint32_t kv_full() const { return bar(0); }
+  __device__ __forceinline__ uint32_t q_full(int s) const { return bar(1 + s); }  // Q_t, nl_t, nd_t landed
+  __device__ __forceinline__ uint32_t do_full(int s) const { return bar(1 + STAGES + s); }  // dO_t landed
+  // the dQ_t half staged in Q_t's / dO_t's buffer has been read
+  __device__ __forceinline__ uint32_t q_empty(int s) const { return bar(1 + 2 * STAGES + s); }
+  __device__ __forceinline__ uint32_t do_empty(int s) const { return bar(1 + 3 * STAGES + s); }
+  __device__ __forceinline__ uint32_t s_full() const { return bar(1 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t p_full() const { return bar(2 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t dp_full() const { return bar(3 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t ds_full() const { return bar(4 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t dq_full() const { return bar(5 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t dq_empty() const { return bar(6 + 4 * STAGES); }
+  // warpgroup h has staged its dQ_t half
+  __device__ __forceinline__ uint32_t red_ready(int h) const { return bar(7 + 4 * STAGES + h); }
+  __device__ __forceinline__ uint32_t dkv_done() const { return bar(9 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t drain() const { return bar(10 + 4 * STAGES); }
+};
+
+// Where a backward CTA works: its (batch, head), key tile and the range of query
+// tiles that see it.  Each role computes this inside its own branch (from a
+// volatile read of the CTA index, so the copies are not merged into one value
+// computed before the branch): nothing then stays live across the role's
+// register-budget change.
+struct BwdTile {
+  int bh, k0, kv_limit, i0, n_it;
+};
+template <int BN, int BM, typename Params>
+__device__ __forceinline__ BwdTile bwd_tile(const Params& p) {
+  uint32_t cta;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(cta));
+  BwdTile g;
+  // head-major; within a head the key tiles with the most query tiles first
+  g.bh = static_cast<int>(cta) / p.n_kt;
+  g.k0 = (static_cast<int>(cta) % p.n_kt) * BN;
+  g.kv_limit = p.Nk;
+  if (p.kv_len) g.kv_limit = min(p.Nk, max(0, p.kv_len[g.bh / p.H]));
+  const int n_qt = (p.N + BM - 1) / BM;
+  // first query tile that sees a key of this tile: causal, key k0 is visible to
+  // query rows i >= k0 - qoff + 1
+  g.i0 = p.causal ? max(0, g.k0 - p.qoff + 1) / BM : 0;
+  g.n_it = (g.k0 < g.kv_limit && g.i0 < n_qt) ? n_qt - g.i0 : 0;
+  return g;
+}
 
 template <int STAGES>
 __global__ void __launch_bounds__(384, 1)
@@ -202,60 +276,30 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* kv_full = bars;
-  uint64_t* q_full = kv_full + 1;         // [S] Q_t and its nl / nd rows have landed
-  uint64_t* do_full = q_full + STAGES;    // [S] dO_t has landed
-  uint64_t* q_empty = do_full + STAGES;   // [S] MMA4_t, the last reader of Q_t, is done
-  uint64_t* do_empty = q_empty + STAGES;  // [S] the dQ_t half staged in dO_t's buffer has been read
-  uint64_t* s_full = do_empty + STAGES;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* dp_full = p_full + 1;
-  uint64_t* ds_full = dp_full + 1;
-  uint64_t* dq_full = ds_full + 1;
-  uint64_t* dq_empty = dq_full + 1;
-  uint64_t* red_ready = dq_empty + 1;  // [2] warpgroup h has staged its dQ_t half
-  uint64_t* ds_free = red_ready + 2;     // the dQ_t half staged in the dS buffer has been read
-  uint64_t* dkv_done = ds_free + 1;
-  uint64_t* drain = dkv_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* issued_q = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
   volatile int* issued_do = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // head-major; within a head the key tiles with the most query tiles first
-  const int bh = static_cast<int>(blockIdx.x) / p.n_kt;
-  const int kt = static_cast<int>(blockIdx.x) % p.n_kt;
-  const int b = bh / p.H;
-  const int k0 = kt * L::BN;
-  int kv_limit = p.Nk;
-  if (p.kv_len) kv_limit = min(p.Nk, max(0, p.kv_len[b]));
-  const int n_qt = (p.N + L::BM - 1) / L::BM;
-  // first query tile that sees a key of this tile: causal, key k0 is visible to
-  // query rows i >= k0 - qoff + 1
-  const int i0 = p.causal ? max(0, k0 - p.qoff + 1) / L::BM : 0;
-  const int n_it = (k0 < kv_limit && i0 < n_qt) ? n_qt - i0 : 0;
-
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
+    const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
+    mbar_init(sm.kv_full(), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&do_full[s], 1);
-      mbar_init(&q_empty[s], 1);
-      mbar_init(&do_empty[s], 1);
+      mbar_init(sm.q_full(s), 1);
+      mbar_init(sm.do_full(s), 1);
+      mbar_init(sm.q_empty(s), 1);
+      mbar_init(sm.do_empty(s), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 256);
-    mbar_init(dp_full, 1);
-    mbar_init(ds_full, 256);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 256);
-    mbar_init(&red_ready[0], 128);
-    mbar_init(&red_ready[1], 128);
-    mbar_init(ds_free, 1);
-    mbar_init(dkv_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(sm.s_full(), 1);
+    mbar_init(sm.p_full(), 256);
+    mbar_init(sm.dp_full(), 1);
+    mbar_init(sm.ds_full(), 256);
+    mbar_init(sm.dq_full(), 1);
+    mbar_init(sm.dq_empty(), 256);
+    mbar_init(sm.red_ready(0), 128);
+    mbar_init(sm.red_ready(1), 128);
+    mbar_init(sm.dkv_done(), 1);
+    mbar_init(sm.drain(), 1);
     *abort_flag = 0;
     *issued_q = 0;
     *issued_do = 0;
@@ -275,157 +319,206 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
   constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
 
   if (warp == 0) {
+    reg_lower<BWD_REGS_LOW>();
+    const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
+    const uint32_t sbase = sm.base;
+    const BwdTile g = bwd_tile<L::BN, L::BM>(p);
+    const int bh = g.bh, k0 = g.k0, i0 = g.i0, n_it = g.n_it;
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
     // ------------------------------------------------------------ producer --
     if (lane == 0 && n_it > 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * L::TILE);
+      mbar_arrive_expect_tx(sm.kv_full(), 2 * L::TILE);
 #pragma unroll
       for (int kb = 0; kb < L::KB; ++kb) {
-        tma_load_3d(smem + L::OFF_K + kb * L::COLBLK, &tm_k, kv_full, kb * 64, k0, bh);
-        tma_load_3d(smem + L::OFF_V + kb * L::COLBLK, &tm_v, kv_full, kb * 64, k0, bh);
+        tma_load_3d(sbase + L::OFF_K + kb * L::COLBLK, &tm_k, sm.kv_full(), kb * 64, k0, bh);
+        tma_load_3d(sbase + L::OFF_V + kb * L::COLBLK, &tm_v, sm.kv_full(), kb * 64, k0, bh);
       }
       for (int t = 0; t < n_it; ++t) {
         const int st = t % STAGES;
         const uint32_t eph = ((t / STAGES) - 1) & 1;
         const int q0 = (i0 + t) * L::BM;
-        if (t >= STAGES && !mbar_wait(&q_empty[st], eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(&q_full[st], L::TILE + 1024);
+        if (p.inject == 2 && t == 1) break;  // test hook: starve the consumers after the first tile
+        if (t >= STAGES && !mbar_wait(sm.q_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(sm.q_full(st), L::TILE + 1024);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(smem + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, &q_full[st], kb * 64, q0, bh);
+          tma_load_3d(sbase + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, sm.q_full(st), kb * 64, q0, bh);
         // nl and nd of the tile's 128 queries (rows padded to a multiple of 128)
         const size_t ws = static_cast<size_t>(bh) * p.Np + q0;
-        bulk_load(smem + L::OFF_STAT + st * 1024, p.nl + ws, 512, &q_full[st]);
-        bulk_load(smem + L::OFF_STAT + st * 1024 + 512, p.nd + ws, 512, &q_full[st]);
+        bulk_load(sbase + L::OFF_STAT + st * 1024, p.nl + ws, 512, sm.q_full(st));
+        bulk_load(sbase + L::OFF_STAT + st * 1024 + 512, p.nd + ws, 512, sm.q_full(st));
         *issued_q = t + 1;
-        if (t >= STAGES && !mbar_wait(&do_empty[st], eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(&do_full[st], L::TILE);
+        if (t >= STAGES && !mbar_wait(sm.do_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(sm.do_full(st), L::TILE);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(smem + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, &do_full[st], kb * 64, q0, bh);
+          tma_load_3d(sbase + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, sm.do_full(st), kb * 64, q0, bh);
         *issued_do = t + 1;
       }
     }
+    tc_fence_before();
+    cta_bar_sync<384>();
+    if (lane == 0 && n_it > 0 && *abort_flag) {
+      // an aborted CTA may not exit while copies it issued are still landing
+      bool ok = mbar_wait_drain(sm.kv_full(), 0, DRAIN_NS);
+      const int nq = *issued_q, nd = *issued_do;
+      for (int t = max(0, nq - STAGES); t < nq; ++t)
+        ok &= mbar_wait_drain(sm.q_full(t % STAGES), (t / STAGES) & 1, DRAIN_NS);
+      for (int t = max(0, nd - STAGES); t < nd; ++t)
+        ok &= mbar_wait_drain(sm.do_full(t % STAGES), (t / STAGES) & 1, DRAIN_NS);
+      if (!ok) atomicOr(p.status, ST_DRAIN);
+    }
   } else if (warp == 1) {
+    reg_lower<BWD_REGS_LOW>();
+    const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
+    const uint32_t sbase = sm.base;
+    const int n_it = bwd_tile<L::BN, L::BM>(p).n_it;
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ---------------------------------------------------------- MMA issuer --
     // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
     if (n_it > 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, L::BM, false, false);  // K Q^T, V dO^T
       constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, true, false);       // P^T dO, dS^T Q
       constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, L::BM, true, true);      // K^T dS
-      const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
-      const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
-      const uint32_t sds = smem_u32(smem + L::OFF_DS);
+      // Descriptors of the operand bases; an operand at byte offset `off` from a
+      // base is that descriptor plus off >> 4 (the start-address field is the
+      // low 14 bits and every shared address here is below 2^18, so no carry).
+      const uint64_t d_k = sdesc_sw128(sbase + L::OFF_K, 16, 1024);        // K-major: K, V, Q, dO, dS^T
+      const uint64_t d_v = sdesc_sw128(sbase + L::OFF_V, 16, 1024);
+      const uint64_t d_q = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+      const uint64_t d_do = sdesc_sw128(sbase + L::OFF_DO, 16, 1024);
+      const uint64_t d_ds = sdesc_sw128(sbase + L::OFF_DS, 16, 1024);
+      const uint64_t m_k = sdesc_sw128(sbase + L::OFF_K, L::COLBLK, 1024);  // MN-major: K, Q, dO, dS
+      const uint64_t m_q = sdesc_sw128(sbase + L::OFF_Q, L::COLBLK, 1024);
+      const uint64_t m_do = sdesc_sw128(sbase + L::OFF_DO, L::COLBLK, 1024);
+      const uint64_t m_ds = sdesc_sw128(sbase + L::OFF_DS, L::COLBLK, 1024);
+      constexpr uint32_t TILE16 = L::TILE >> 4;
 
       // S^T = K Q_t^T or dP^T = V dO_t^T: both operands K-major, two column blocks each
-      auto mma_scores = [&](uint32_t d_tm, uint32_t a_base, uint32_t b_base) {
+      auto mma_scores = [&](uint32_t d_tm, uint64_t a, uint64_t b) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::COLBLK + (kk & 3) * 32;
-          umma_ss_w(d_tm, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), IDESC_S,
-                  kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
+          umma_ss_w(d_tm, a + off, b + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
       // Issue order: MMA1_0, MMA2_0, then per tile t
-      //   MMA3_t, MMA1_{t+1}, MMA4_t, MMA5_t, MMA2_{t+1}
-      // so that S^T_{t+1} is ready while the warpgroups finish tile t, and
-      // MMA4_t / MMA5_t run while they form P^T_{t+1}.
-      bool ok = mbar_wait_w(kv_full, 0, wc, ST_BWD_TIMEOUT_KV) && mbar_wait_w(&q_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
+      //   MMA3_t, MMA4_t, MMA5_t, MMA1_{t+1}, MMA2_{t+1}
+      bool ok = mbar_wait_w(sm.kv_full(), 0, wc, ST_BWD_TIMEOUT_KV) && mbar_wait_w(sm.q_full(0), 0, wc, ST_BWD_TIMEOUT_Q);
       if (ok) {
         tc_fence_after();
-        mma_scores(tmem + L::TM_S, sk, sq);
-        umma_commit_w(s_full);
-        ok = mbar_wait_w(&do_full[0], 0, wc, ST_BWD_TIMEOUT_Q);
+        mma_scores(tmem + L::TM_S, d_k, d_q);
+        umma_commit_w(sm.s_full());
+        ok = mbar_wait_w(sm.do_full(0), 0, wc, ST_BWD_TIMEOUT_Q);
       }
       if (ok) {
         tc_fence_after();
-        mma_scores(tmem + L::TM_DP, sv, sdo);
-        umma_commit_w(dp_full);
+        mma_scores(tmem + L::TM_DP, d_v, d_do);
+        umma_commit_w(sm.dp_full());
       }
       for (int t = 0; ok && t < n_it; ++t) {
         const int st = t % STAGES, st1 = (t + 1) % STAGES;
         const uint32_t ph = t & 1, ph1 = ((t + 1) / STAGES) & 1;
-        const uint32_t q_t = sq + st * L::TILE, do_t = sdo + st * L::TILE;
         const bool next = t + 1 < n_it;
         // MMA3: dV += P^T_t dO_t.  A = P^T from tensor memory: queries 0-63 in
         // columns [0, 32), queries 64-127 in [64, 96) (each half in its own
         // S columns); B = dO_t MN-major (16 queries = 2 KB per step).
-        if (!mbar_wait_w(p_full, ph, wc, ST_BWD_TIMEOUT_P)) break;
+        if (!mbar_wait_w(sm.p_full(), ph, wc, ST_BWD_TIMEOUT_P)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < L::BM / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + pcol, sdesc_sw128(do_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
+          umma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + pcol, m_do + st * TILE16 + kk * (2048 >> 4), IDESC_G,
                   (t > 0 || kk > 0) ? 1u : 0u);
         }
-        // MMA1: S^T_{t+1} into the S columns.  P^T_t is read by MMA3_t, issued
-        // just before (the tensor cores run in issue order).
-        if (next) {
-          if (!mbar_wait_w(&q_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
-          tc_fence_after();
-          mma_scores(tmem + L::TM_S, sk, sq + st1 * L::TILE);
-          umma_commit_w(s_full);
-        }
-        if (!mbar_wait_w(ds_full, ph, wc, ST_BWD_TIMEOUT_DS)) break;
+        if (!mbar_wait_w(sm.ds_full(), ph, wc, ST_BWD_TIMEOUT_DS)) break;
         tc_fence_after();
         // MMA4: dK += dS^T_t Q_t.  A = dS^T (bf16) from the dP columns, laid out
         // like P^T; B = Q_t MN-major.
 #pragma unroll
         for (int kk = 0; kk < L::BM / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_ts_w(tmem + L::TM_DK, tmem + L::TM_DP + pcol, sdesc_sw128(q_t + kk * 2048, L::COLBLK, 1024), IDESC_G,
+          umma_ts_w(tmem + L::TM_DK, tmem + L::TM_DP + pcol, m_q + st * TILE16 + kk * (2048 >> 4), IDESC_G,
                   (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit_w(&q_empty[st]);
         // MMA5: dQ^T_t = K^T dS_t into the dP columns, after MMA4 has read dS^T
         // there.  A = K MN-major, B = dS^T read as [query][key] MN-major (two
         // 64-query blocks, 16 KB apart).
 #pragma unroll
         for (int kk = 0; kk < L::BN / 16; ++kk)
-          umma_ss_w(tmem + L::TM_DP, sdesc_sw128(sk + kk * 2048, L::COLBLK, 1024),
-                  sdesc_sw128(sds + kk * 2048, L::COLBLK, 1024), IDESC_Q, kk > 0 ? 1u : 0u);
-        umma_commit_w(dq_full);  // also MMA4_t: dO_t's buffer and the dS buffer are free
-        // MMA2: dP^T_{t+1} into the dP columns once dQ^T_t has been drained
+          umma_ss_w(tmem + L::TM_DP, m_k + kk * (2048 >> 4), m_ds + kk * (2048 >> 4), IDESC_Q, kk > 0 ? 1u : 0u);
+        // also MMA1_t .. MMA4_t: Q_t's and dO_t's buffers are free for the dQ staging
+        umma_commit_w(sm.dq_full());
         if (next) {
-          if (!mbar_wait_w(dq_empty, ph, wc, ST_BWD_TIMEOUT_DQE)) break;
-          if (!mbar_wait_w(&do_full[st1], ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          // MMA1: S^T_{t+1} into the S columns (P^T_t was read by MMA3_t, issued
+          // before: the tensor cores run in issue order).
+          if (!mbar_wait_w(sm.q_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) break;
           tc_fence_after();
-          mma_scores(tmem + L::TM_DP, sv, sdo + st1 * L::TILE);
-          umma_commit_w(dp_full);
+          mma_scores(tmem + L::TM_S, d_k, d_q + st1 * TILE16);
+          umma_commit_w(sm.s_full());
+          // MMA2: dP^T_{t+1} into the dP columns once dQ^T_t has been read out.
+          // Its commit also covers MMA5_t, the last reader of the dS buffer.
+          if (!mbar_wait_w(sm.dq_empty(), ph, wc, ST_BWD_TIMEOUT_DQE)) break;
+          if (!mbar_wait_w(sm.do_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          tc_fence_after();
+          mma_scores(tmem + L::TM_DP, d_v, d_do + st1 * TILE16);
+          umma_commit_w(sm.dp_full());
         }
       }
-      umma_commit_w(dkv_done);
+      umma_commit_w(sm.dkv_done());
       // nothing may be in flight on the tensor cores when the CTA frees TMEM
-      umma_commit_w(drain);
-      if (!mbar_wait_drain(drain, 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
+      umma_commit_w(sm.drain());
+      if (!mbar_wait_drain(sm.drain(), 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
     }
+    tc_fence_before();
+    cta_bar_sync<384>();
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TM_COLS);
   } else if (warp == 2) {
+    reg_lower<BWD_REGS_LOW>();
+    const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
+    const uint32_t sbase = sm.base;
+    const BwdTile g = bwd_tile<L::BN, L::BM>(p);
+    const int bh = g.bh, i0 = g.i0, n_it = g.n_it;
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
     // ----------------------------------------------------- dQ reduce-adds --
-    // Per tile: the half staged in the dS buffer first (the warpgroups need the
-    // buffer back for dS^T_{t+1}), then the half in dO_t's buffer.
+    // Per tile: the half staged in Q_t's buffer (queries 64-127) first, then the
+    // half in dO_t's buffer (0-63); each buffer goes back to the producer once
+    // its reduce-add has read it.  Q_{t+2} is needed sooner than dO_{t+2} (its
+    // S^T product comes first), so Q_t's buffer is released first.  A reduce-add
+    // reads its 32 KB at about 25 bytes per cycle (the SM's rate for reductions
+    // into global memory), so the two take about as long as the tile's products.
     if (lane == 0 && n_it > 0) {
       for (int t = 0; t < n_it; ++t) {
         const int st = t % STAGES;
         const int q0 = (i0 + t) * L::BM;
-        if (!mbar_wait(&red_ready[1], t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
-        tma_reduce_add_3d(&tm_dq, smem + L::OFF_DS, 0, q0 + 64, bh);
+        if (!mbar_wait(sm.red_ready(1), t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
+        tma_reduce_add_3d(&tm_dq, sbase + L::OFF_Q + st * L::TILE, 0, q0 + 64, bh);
         bulk_commit_group();
-        if (!mbar_wait(&red_ready[0], t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
-        tma_reduce_add_3d(&tm_dq, smem + L::OFF_DO + st * L::TILE, 0, q0, bh);
+        if (!mbar_wait(sm.red_ready(0), t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
+        tma_reduce_add_3d(&tm_dq, sbase + L::OFF_DO + st * L::TILE, 0, q0, bh);
         bulk_commit_group();
         bulk_wait_read<1>();
-        mbar_arrive(ds_free);
+        mbar_arrive(sm.q_empty(st));
         bulk_wait_read<0>();
-        mbar_arrive(&do_empty[st]);
+        mbar_arrive(sm.do_empty(st));
       }
       // the CTA may not exit while a reduce-add still reads its shared memory
       bulk_wait_all();
     }
+    cta_bar_sync<384>();
   } else if (warp >= 4) {
+    reg_raise<BWD_REGS_HIGH>();
+    const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
+    const uint32_t sbase = sm.base;
+    const BwdTile g = bwd_tile<L::BN, L::BM>(p);
+    const int bh = g.bh, k0 = g.k0, kv_limit = g.kv_limit, i0 = g.i0, n_it = g.n_it;
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ---------------------------------------------------- elementwise WGs --
     // Both warpgroups take every tile: warpgroup h owns query columns
     // [64 h, 64 h + 64).  Thread r is key row r (TMEM lane r) of S^T and dP^T,
@@ -438,21 +531,55 @@ __global__ void __launch_bounds__(384, 1)
     const bool key_ok = (k0 + r) < kv_limit;
     const int jrow = k0 + r - p.qoff + 1;  // causal: first visible query row of key k0 + r
     const float sl = p.scale_log2, scale = p.scale;
-    const uint32_t ds_row = smem_u32(smem + L::OFF_DS) + h * L::COLBLK + r * 128;
-    const uint32_t stat = smem_u32(smem + L::OFF_STAT) + h * 256;  // + stage * 1024: nl; + 512: nd
+    const uint32_t ds_row = sbase + L::OFF_DS + h * L::COLBLK + r * 128;
+    const uint32_t stat = sbase + L::OFF_STAT + h * 256;  // + stage * 1024: nl; + 512: nd
     bool ok = true;
-    float pr[64];
-    // Pass t forms P^T and dS^T of tile u = t + 1 around the drain of dQ^T_t:
-    //   P^T_u  |  dQ^T_t -> staged row-major for its reduce-add  |  dS^T_u
+    // Pass t drains dQ^T_t, then forms P^T and dS^T of tile u = t + 1:
+    //   dQ^T_t -> staged row-major for its reduce-add  |  P^T_u  |  dS^T_u
+    // (dS^T_u waits for dP^T_u, which MMA2_u writes only after the drain, so
+    // P^T_u fits in that wait either way; this order keeps P^T_u's registers
+    // out of the drain.)
     for (int t = -1; t < n_it; ++t) {
+      float pr[64];  // P^T_u of this thread's key row, from the first part to the last
       const int u = t + 1;
       const int su = u % STAGES;
       const int qu = (i0 + u) * L::BM + h * 64;  // first query of this half of tile u
+      if (t >= 0) {
+        // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows.
+        // Stage them row-major -- warpgroup 0 in dO_t's buffer, warpgroup 1 in
+        // Q_t's buffer, both free since every reader of Q_t and dO_t ran before
+        // MMA5_t -- for one tiled reduce-add into global dQ each (rows past N are
+        // skipped by the tensor map).  A warp's 32 lanes write 128 consecutive
+        // bytes per store; after the second load the dP columns are free for
+        // MMA2_{t+1}.
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), t & 1, wc, ST_BWD_TIMEOUT_DQ))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t out_row = sbase + (h == 0 ? L::OFF_DO : L::OFF_Q) + (t % STAGES) * L::TILE + r * 4;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t qr[32];
+          FA_TMEM_LD32(dp_col + half * 32, qr);
+          tmem_wait_ld();
+          FA_REG_FENCE32(qr);
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(sm.dq_empty());
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) st_shared_f32(out_row + (half * 32 + j) * 512, __uint_as_float(qr[j]));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(sm.red_ready(h));
+      }
+
       if (u < n_it) {
         // q_full is already complete here (S^T_u exists); waiting on it makes the
         // stage's nl / nd rows visible to these threads
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full, u & 1, wc, ST_BWD_TIMEOUT_S) &&
-                                         mbar_wait(&q_full[su], (u / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.s_full(), u & 1, wc, ST_BWD_TIMEOUT_S) &&
+                                         mbar_wait(sm.q_full(su), (u / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
           ok = false;
           break;
         }
@@ -480,12 +607,17 @@ __global__ void __launch_bounds__(384, 1)
             ld_shared_v4f(nl_s + (half * 32 + j4) * 4, nl);
 #pragma unroll
             for (int w = 0; w < 4; w += 2) {
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
-                               f2_pack(nl[w], nl[w + 1])),
-                        x0, x1);
-              pr[half * 32 + j4 + w] = ex2_approx(x0);
-              pr[half * 32 + j4 + w + 1] = ex2_approx(x1);
+              const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
+                                         f2_pack(nl[w], nl[w + 1]));
+              constexpr int E = FA_BWD_EXP2_FMA_EVERY > 0 ? FA_BWD_EXP2_FMA_EVERY : 1;
+              if (FA_BWD_EXP2_FMA_EVERY > 0 && ((j4 + w) / 2 + 1) % E == 0) {
+                f2_unpack(exp2_fma2(x2), pr[half * 32 + j4 + w], pr[half * 32 + j4 + w + 1]);  // FMA pipe
+              } else {
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                pr[half * 32 + j4 + w] = ex2_approx(x0);
+                pr[half * 32 + j4 + w + 1] = ex2_approx(x1);
+              }
             }
           }
         }
@@ -495,42 +627,12 @@ __global__ void __launch_bounds__(384, 1)
         FA_TMEM_ST32(s_col, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_full);
-      }
-
-      if (t >= 0) {
-        // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows.
-        // Stage them row-major -- warpgroup 0 in dO_t's buffer, warpgroup 1 in
-        // the dS buffer, both free once MMA5_t (the last MMA of tile t) has run --
-        // for one tiled reduce-add into global dQ (rows past N are skipped by
-        // the tensor map).  A warp's 32 lanes write 128 consecutive bytes per
-        // store.  32 columns at a time keeps P^T_u's registers live alongside.
-        if (!__all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, wc, ST_BWD_TIMEOUT_DQ))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t out_row =
-            smem_u32(smem + (h == 0 ? L::OFF_DO + (t % STAGES) * L::TILE : L::OFF_DS)) + r * 4;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t qr[32];
-          FA_TMEM_LD32(dp_col + half * 32, qr);
-          tmem_wait_ld();
-          FA_REG_FENCE32(qr);
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(dq_empty);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) st_shared_f32(out_row + (half * 32 + j) * 512, __uint_as_float(qr[j]));
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&red_ready[h]);
+        mbar_arrive(sm.p_full());
       }
 
       if (u < n_it) {
-        if (!__all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, wc, ST_BWD_TIMEOUT_DP))) {
+        // dP^T_u; its commit also covers MMA5_t, so the dS buffer is free
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.dp_full(), u & 1, wc, ST_BWD_TIMEOUT_DP))) {
           ok = false;
           break;
         }
@@ -562,28 +664,24 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
-        // The dS buffer is free once the dQ^T_t half staged there has been read.
-        if (t >= 0 && !__all_sync(0xffffffffu, mbar_wait(ds_free, t & 1, wc, ST_BWD_TIMEOUT_RED))) {
-          ok = false;
-          break;
-        }
         // dS^T as MMA4's A operand: bf16 pairs into the first 32 of this half's
-        // dP columns (dP^T has been read into registers)
+        // dP columns (dP^T has been read into registers) ...
         FA_TMEM_ST32(dp_col, dsk);
-        // Row r of this half's 128B-swizzled block: 16-byte chunk c lands at c ^ (r & 7).
+        // ... and as MMA5's B operand: row r of this half's 128B-swizzled block,
+        // 16-byte chunk c at c ^ (r & 7).
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
-        mbar_arrive(ds_full);
+        mbar_arrive(sm.ds_full());
       }
     }
 
     // ------------------------------------------------------------ epilogue --
     // warpgroup 0 writes dV, warpgroup 1 writes dK: TMEM lane r = key row k0 + r
-    if (ok && n_it > 0 && !__all_sync(0xffffffffu, mbar_wait(dkv_done, 0, wc, ST_BWD_TIMEOUT_DONE))) ok = false;
+    if (ok && n_it > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.dkv_done(), 0, wc, ST_BWD_TIMEOUT_DONE))) ok = false;
     if (ok) {
       tc_fence_after();
       const int key = k0 + r;
@@ -609,23 +707,11 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0 && lane == 0 && n_it > 0 && *abort_flag) {
-    // an aborted CTA may not exit while copies it issued are still landing
-    bool ok = mbar_wait_drain(kv_full, 0, DRAIN_NS);
-    const int nq = *issued_q, nd = *issued_do;
-    for (int t = max(0, nq - STAGES); t < nq; ++t)
-      ok &= mbar_wait_drain(&q_full[t % STAGES], (t / STAGES) & 1, DRAIN_NS);
-    for (int t = max(0, nd - STAGES); t < nd; ++t)
-      ok &= mbar_wait_drain(&do_full[t % STAGES], (t / STAGES) & 1, DRAIN_NS);
-    if (!ok) atomicOr(p.status, ST_DRAIN);
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, L::TM_COLS);
+    tc_fence_before();
+    cta_bar_sync<384>();
+  } else {
+    reg_lower<BWD_REGS_LOW>();  // warp 3: no role
+    cta_bar_sync<384>();
   }
 }
 

@@ -22,8 +22,12 @@
 
 namespace fa {
 // Status word of the current device: kernels OR their timeout codes into it;
-// fa_check_device_error reads and clears it.
+// fa_check_device_error takes it (reads and clears it in one atomic exchange).
 __device__ unsigned int g_status_word;
+// Where the exchange leaves the word it took, for the host to copy back.
+__device__ unsigned int g_status_taken;
+
+__global__ void status_take_kernel(unsigned int* status, unsigned int* taken) { *taken = atomicExch(status, 0u); }
 }  // namespace fa
 
 namespace {
@@ -52,23 +56,62 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 
 struct DeviceState {
   bool ready = false;
+  unsigned long long ctx_id = 0;   // the CUDA context the fields below belong to
   int cc_major = 0, cc_minor = 0;
   unsigned int* status = nullptr;  // device address of fa::g_status_word
+  unsigned int* taken = nullptr;   // device address of fa::g_status_taken
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// Per-device set-up, done once with that device current: read the compute
-// capability, resolve the status word's device address, raise the kernels'
-// dynamic shared-memory limit.
+using PFN_ctx_get_current = CUresult (*)(CUcontext*);
+using PFN_ctx_get_id = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (creating the device's
+// primary context if none is current yet).  Device addresses of the library's
+// variables and the kernels' attributes belong to one context: after a
+// cudaDeviceReset the caller gets a new context and they are set up again.
+fa_status current_context_id(int dev, unsigned long long* id) {
+  static PFN_ctx_get_current get_current = nullptr;
+  static PFN_ctx_get_id get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_ctx_get_current>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_ctx_get_id>(p);
+  });
+  if (!get_current || !get_id) return fail(FA_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId unavailable from the driver");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (!ctx) {
+    cudaError_t e = cudaSetDevice(dev);  // makes the device's primary context current
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return fail(FA_ERR_CUDA, "no CUDA context after cudaSetDevice");
+  }
+  if (get_id(ctx, id) != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuCtxGetId failed");
+  return FA_OK;
+}
+
+// Per-device set-up, done with that device current, once per CUDA context: read
+// the compute capability, resolve the status words' device addresses, raise
+// the kernels' dynamic shared-memory limit.
 fa_status device_state(DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  unsigned long long ctx_id = 0;
+  fa_status st = current_context_id(dev, &ctx_id);
+  if (st != FA_OK) return st;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceState& s = g_dev[dev];
-  if (!s.ready) {
+  if (!s.ready || s.ctx_id != ctx_id) {
+    s.ready = false;
     if ((e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if ((e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
@@ -80,6 +123,9 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaGetSymbolAddress(&addr, fa::g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
     s.status = static_cast<unsigned int*>(addr);
+    if ((e = cudaGetSymbolAddress(&addr, fa::g_status_taken)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status copy)");
+    s.taken = static_cast<unsigned int*>(addr);
     using L128 = fa::TcLayout<128, kSlotsD128>;
     using L64 = fa::TcLayout<64, kSlotsD64>;
     if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<128, kSlotsD128>,
@@ -91,6 +137,7 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fa::BwdLayout<kStagesBwd>::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+    s.ctx_id = ctx_id;
     s.ready = true;
   }
   *out = &s;
@@ -233,6 +280,16 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   const long long blocks = n_kt * BH;
   if (pre_blocks > 0x7fffffffll || blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
 
+  // every tensor map is built before anything is enqueued, so that a failure
+  // here leaves the stream untouched
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  fa_status s;
+  if ((s = make_map(&mq, q, D, N, BH, "q", 128)) != FA_OK) return s;
+  if ((s = make_map(&mk, k, D, Nk, BH, "k", 128)) != FA_OK) return s;
+  if ((s = make_map(&mv, v, D, Nk, BH, "v", 128)) != FA_OK) return s;
+  if ((s = make_map(&mdo, dO, D, N, BH, "dO", 128)) != FA_OK) return s;
+  if ((s = make_map_f32(&mdq, dq, D, N, BH, "dq", 64)) != FA_OK) return s;
+
   fa::BwdPreParams pp{};
   pp.o = static_cast<const __nv_bfloat16*>(o);
   pp.dO = static_cast<const __nv_bfloat16*>(dO);
@@ -248,13 +305,6 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch bwd_preprocess_kernel");
 
-  CUtensorMap mq, mk, mv, mdo, mdq;
-  fa_status s;
-  if ((s = make_map(&mq, q, D, N, BH, "q", 128)) != FA_OK) return s;
-  if ((s = make_map(&mk, k, D, Nk, BH, "k", 128)) != FA_OK) return s;
-  if ((s = make_map(&mv, v, D, Nk, BH, "v", 128)) != FA_OK) return s;
-  if ((s = make_map(&mdo, dO, D, N, BH, "dO", 128)) != FA_OK) return s;
-  if ((s = make_map_f32(&mdq, dq, D, N, BH, "dq", 64)) != FA_OK) return s;
   fa::BwdParams p{};
   p.dq = dq;
   p.dk = dk;
@@ -274,6 +324,7 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.qoff = causal_qoff(N, Nk, causal);
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
+  p.inject = g_inject.load();
   fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_bf16_tc_kernel");
   return FA_OK;
@@ -458,17 +509,25 @@ const char* fa_last_error_string(void) { return t_err; }
 
 fa_status fa_check_device_error(void* stream) {
   t_err[0] = '\0';
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   DeviceState* ds = nullptr;
   fa_status s = device_state(&ds);
   if (s != FA_OK) return s;
-  unsigned int word = 0, zero = 0;
-  if ((e = cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
-    return cuda_fail(e, "read status word");
+  // Take the word (read and clear in one atomic exchange on the device, so a bit
+  // a kernel on another stream sets meanwhile is never lost), then copy it back.
+  unsigned int word = 0;
+  {
+    static std::mutex take_mu;  // one copy-back slot per device
+    std::lock_guard<std::mutex> lk(take_mu);
+    fa::status_take_kernel<<<1, 1, 0, st>>>(ds->status, ds->taken);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch status_take_kernel");
+    if ((e = cudaMemcpyAsync(&word, ds->taken, sizeof(word), cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+      return cuda_fail(e, "read status word");
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  }
   if (word == 0) return FA_OK;
-  if ((e = cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
-    return cuda_fail(e, "clear status word");
   if (word & fa::ST_BWD_SMEM_ALIGN)
     return fail(FA_ERR_CUDA, "backward kernel found its shared memory base misaligned and did nothing (status bits "
                 "0x%x)", word);
@@ -509,22 +568,27 @@ namespace {
 static __device__ __align__(256) float g_bwd_noalloc_scratch[2 * FA_BWD_NOALLOC_MAX_ROWS];
 
 float* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
-// The array's device address for the current device, looked up once per device
-// with that device current (the host-side name of the array is only a stand-in
-// and must never be handed to a kernel).
+// The array's device address for the current device, looked up with that
+// device current, again whenever the CUDA context has changed (the host-side
+// name of the array is only a stand-in and must never be handed to a kernel).
 fa_status noalloc_scratch(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  unsigned long long ctx_id = 0;
+  fa_status st = current_context_id(dev, &ctx_id);
+  if (st != FA_OK) return st;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx_id) {
     void* addr = nullptr;
     if ((e = cudaGetSymbolAddress(&addr, g_bwd_noalloc_scratch)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(backward scratch)");
     g_noalloc_ptr[dev] = static_cast<float*>(addr);
+    g_noalloc_ctx[dev] = ctx_id;
   }
   *out = g_noalloc_ptr[dev];
   return FA_OK;

@@ -32,13 +32,31 @@
 //
 // Rescaling is lazy: a row's reference m moves only when a block's max exceeds it
 // by more than 8 (base 2).  l and acc always share the reference, so acc / l is
-// unchanged -- the cancellation of the Exercises page ("top and bottom both get
-// multiplied by e^-m") -- and the O round trip through tensor memory happens
-// only for blocks that move the reference.  Terms stay below 2^8.
+// unchanged -- the cancellation argument of the Exercises page: numerator and
+// denominator carry the same factor e^-m -- and the O round trip through tensor
+// memory happens only for blocks that move the reference.  Terms stay below 2^8.
 #pragma once
+#include "exp2_poly.cuh"
 #include "ptx.cuh"
 
+// Every FA_FWD_EXP2_FMA_EVERY-th pair of scores takes its exponentials on the FMA
+// pipe (exp2_fma2) instead of the special-function unit; 0 = none.
+#ifndef FA_FWD_EXP2_FMA_EVERY
+#define FA_FWD_EXP2_FMA_EVERY 0
+#endif
+
 namespace fa {
+
+// Pair i of each 16-pair quarter of a row takes the FMA-pipe exponential.
+__host__ __device__ constexpr bool exp2_on_fma(int i) {
+  return FA_FWD_EXP2_FMA_EVERY > 0 && (i + 1) % (FA_FWD_EXP2_FMA_EVERY > 0 ? FA_FWD_EXP2_FMA_EVERY : 1) == 0;
+}
+
+// Register shares (launch: 384 threads x 168): warpgroup 2 (producer, MMA issuer,
+// two idle warps) keeps FWD_REGS_LOW, the two softmax warpgroups get
+// FWD_REGS_HIGH; 128 x 56 + 256 x 208 = 60416 <= 64512.
+constexpr uint32_t FWD_REGS_LOW = 56, FWD_REGS_HIGH = 208;
+static_assert(128 * FWD_REGS_LOW + 256 * FWD_REGS_HIGH <= 384 * 168, "register split exceeds the launch");
 
 // Bits of the global status word (a timeout names the barrier it gave up on).
 enum : unsigned {
@@ -166,6 +184,7 @@ __global__ void __launch_bounds__(384, 1)
   // that it holds no register in the other roles
   volatile int* issued = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
   if (warp == 8) {
+    reg_lower<FWD_REGS_LOW>();
     // ------------------------------------------------------------ producer --
     if (lane == 0 && n_max > 0) {
       const int nq = (n_t1 > 0) ? 2 : 1;
@@ -188,6 +207,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 9) {
+    reg_lower<FWD_REGS_LOW>();
     // ---------------------------------------------------------- MMA issuer --
     // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
     if (n_max > 0) {
@@ -276,6 +296,7 @@ __global__ void __launch_bounds__(384, 1)
       if (!mbar_wait_drain(drain, 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
     }
   } else if (warp < 8) {
+    reg_raise<FWD_REGS_HIGH>();
     // ------------------------------------------------------------- softmax --
     const int ti = warp >> 2;          // query tile 0 or 1 (warps 10-11 have no role)
     const int r = threadIdx.x & 127;   // row in the tile == tensor-memory lane
@@ -287,7 +308,10 @@ __global__ void __launch_bounds__(384, 1)
     const int n_kv = ti ? n_t1 : n_t0;
     const int qt0c = q0 + ti * L::BM + p.qoff;  // qlim of the tile's first row
     const float sl = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    // l: the row sum of the probabilities as computed (float32), for lse;
+    // dl: how much the bf16 values the P V product uses differ from them, for
+    // the largest probability of each block (see below)
+    float m = -INFINITY, l = 0.f, dl = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       // tcgen05.ld/st are warp-collective: the whole warp goes on or stops together
@@ -330,6 +354,13 @@ __global__ void __launch_bounds__(384, 1)
       const float m_new = (m_blk > m + 8.f) ? m_blk : m;  // lazy reference move
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float c = ex2_approx(m - m_ref);               // 0 on the first block, 1 if unchanged
+      // The product O += P V sees P rounded to bf16.  A row whose weight sits on
+      // one key (large logits) then has O = v (p~ / p): off by up to 2^-9 |v|
+      // when p is normalised by the float32 sum.  Adding p~ - p of each block's
+      // largest probability (the same fma and ex2 as below, so the same bits)
+      // to the normaliser of O makes that term exact; lse keeps the float32 sum.
+      const float p_mx = ex2_approx(fmaf(mx, sl, -m_ref));
+      dl = dl * c + (__bfloat162float(__float2bfloat16_rn(p_mx)) - p_mx);
       // x = s * scale*log2(e) - m_ref two scores at a time (f32x2), p = 2^x, row
       // sum in 4 independent chains; P in quarters of 32 scores (16 packed
       // columns) keeps register use low
@@ -341,12 +372,19 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[32 * h + 2 * i]), __uint_as_float(sr[32 * h + 2 * i + 1])),
-                           sl2, nm2),
-                    x0, x1);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          rs2[i & 1] = f2_add(rs2[i & 1], f2_pack(p0, p1));
+          const uint64_t x2 =
+              f2_fma(f2_pack(__uint_as_float(sr[32 * h + 2 * i]), __uint_as_float(sr[32 * h + 2 * i + 1])), sl2, nm2);
+          uint64_t p2;
+          if (exp2_on_fma(i)) {
+            p2 = exp2_fma2(x2);  // this pair on the FMA pipe
+          } else {
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          }
+          rs2[i & 1] = f2_add(rs2[i & 1], p2);
+          float p0, p1;
+          f2_unpack(p2, p0, p1);
           pk[i] = pack_bf16x2(p0, p1);
         }
         FA_TMEM_ST16(s_col + 16 * h, pk);
@@ -379,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
     const int qrow = qlim - p.qoff;
     if (ok && qt0c - p.qoff < p.N) {
       tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;  // guard: l = 0 -> zero vector
+      const float inv = (l > 0.f) ? 1.f / (l + dl) : 0.f;  // guard: l = 0 -> zero vector
       const size_t orow = (static_cast<size_t>(bh) * p.N + qrow) * D;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
@@ -405,6 +443,8 @@ __global__ void __launch_bounds__(384, 1)
       if (p.lse && qrow < p.N)
         p.lse[static_cast<size_t>(bh) * p.N + qrow] = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
+  } else {
+    reg_lower<FWD_REGS_LOW>();  // warps 10-11: no role
   }
 
   tc_fence_before();

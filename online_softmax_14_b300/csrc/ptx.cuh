@@ -13,6 +13,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The same conversion in a volatile asm: every call is a separate value, so a
+// role of a warp-specialised kernel can take its own copy after changing its
+// register budget instead of keeping one from before the change live.
+__device__ __forceinline__ uint32_t smem_u32_fresh(const void* p) {
+  uint32_t a;
+  asm volatile("{\n\t.reg .u64 t;\n\tcvta.to.shared.u64 t, %1;\n\tcvt.u32.u64 %0, t;\n\t}" : "=r"(a) : "l"(p));
+  return a;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -20,19 +29,27 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------- mbarrier ---
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+// Barriers are named by their 32-bit shared-memory address (smem_u32); the
+// pointer forms below convert and forward.  Kernels with many barriers keep
+// the addresses as 32-bit values so that warps with small register budgets do
+// not hold 64-bit pointers.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) { mbar_init(smem_u32(bar), count); }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) { mbar_arrive(smem_u32(bar)); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
+  mbar_arrive_expect_tx(smem_u32(bar), bytes);
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -57,8 +74,7 @@ struct WaitCtl {
 // Wait until the phase with the given parity has completed.  Returns false if the
 // CTA was told to abort or the wait ran past the time limit (which then records
 // `code` in the status word and raises the abort flag).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w, unsigned code) {
-  const uint32_t a = smem_u32(bar);
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const WaitCtl& w, unsigned code) {
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -76,8 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 
 // mbar_wait for a whole converged warp: every lane tests the barrier and the
 // outcome is made warp-uniform (a phase, once complete, stays complete).
-__device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, const WaitCtl& w, unsigned code) {
-  const uint32_t a = smem_u32(bar);
+__device__ __forceinline__ bool mbar_wait_w(uint32_t a, uint32_t parity, const WaitCtl& w, unsigned code) {
   if (__any_sync(0xffffffffu, mbar_try_wait(a, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -97,13 +112,21 @@ __device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, cons
 
 // Wait with a limit, ignoring the abort flag: used only while draining work that
 // is already in flight before a CTA exits.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint32_t a = smem_u32(bar);
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t a, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(a, parity)) {
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w, unsigned code) {
+  return mbar_wait(smem_u32(bar), parity, w, code);
+}
+__device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, const WaitCtl& w, unsigned code) {
+  return mbar_wait_w(smem_u32(bar), parity, w, code);
+}
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return mbar_wait_drain(smem_u32(bar), parity, limit_ns);
 }
 
 // -------------------------------------------------------------------- TMA ---
@@ -113,21 +136,23 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
 
 // 3-D tiled load global -> shared, completion counted in bytes on `bar`.
 // x (innermost coordinate, elements) must make x * sizeof(elem) a multiple of 16.
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+  tma_load_3d(smem_u32(dst), m, smem_u32(bar), x, y, z);
 }
 
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.  Both
 // addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -143,11 +168,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // 3-D tiled reduce-add shared -> global (element-wise atomic add of the box at
 // the given coordinates), tracked by this thread's bulk async-group.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
   asm volatile(
       "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(m)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -219,13 +244,14 @@ __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 // Lane 0 (the lane that issued the MMAs) arrives once on `bar` when every
 // tcgen05.mma it has issued so far is done.
-__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+__device__ __forceinline__ void umma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
       "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) { umma_commit_w(smem_u32(bar)); }
 
 // Instruction descriptor, kind::f16 with bf16 A and B, f32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
@@ -293,6 +319,32 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
                  "+r"((r)[24]), "+r"((r)[25]), "+r"((r)[26]), "+r"((r)[27]), "+r"((r)[28]), "+r"((r)[29]),    \
                  "+r"((r)[30]), "+r"((r)[31]))
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Barrier 1 across all `nthreads` threads of the CTA, executed from inside a
+// role's own branch.  Warp-specialised kernels end each role with it (instead of
+// one __syncthreads after the branches join), so that no value has to stay live
+// into a join shared by roles with different register budgets.
+// The warp reconverges first: bar.sync is warp-aligned, and some roles reach it
+// after work done by one lane.
+template <int nthreads>
+__device__ __forceinline__ void cta_bar_sync() {
+  __syncwarp();
+  asm volatile("bar.sync 1, %0;" ::"n"(nthreads) : "memory");
+}
+
+// Per-warp register budget of a warp-specialised kernel: a warp's role lowers
+// or raises its share of the registers the CTA was launched with.  Every warp of
+// a warpgroup takes the same value; the raised and lowered shares must add up
+// to no more than the launch's registers (threads x registers per thread), or
+// the raise would wait for registers that never come.
+template <uint32_t N>
+__device__ __forceinline__ void reg_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------- ALU ---
 // Packed pair of floats in one 64-bit register: the sm_100 family's f32x2

@@ -23,10 +23,10 @@ Two forms of the same algorithm, each in the pages' notation:
   removes the factor c, the page's red-team mutation, which must break exactness.
 
 The division is guarded: l == 0 (every key masked) returns the zero vector
-(Worked examples, Cell D2).  Where both maxima are -inf the pages say the merge
-"still runs, every term is zero"; with IEEE arithmetic exp(-inf - (-inf)) is NaN,
-so the common reference is taken as 0 when m_new = -inf, which makes every term
-exactly 0 as the page describes.
+(Worked examples, Cell D2).  Where both maxima are -inf, Cell D2 lets the merge
+go ahead with every term equal to zero; with IEEE arithmetic exp(-inf - (-inf))
+is NaN, so the common reference is taken as 0 when m_new = -inf, which makes
+every term exactly 0 as the page describes.
 """
 
 from __future__ import annotations

@@ -37,8 +37,11 @@ def run_fwd_bwd(pr, causal, kv_len=None):
 # Large-logit inputs (Q, K x 8) give gradients of magnitude ~25; there the bar
 # is relative to the largest oracle gradient.  The kernel rounds P and dS to
 # bf16 (relative error <= 2^-9 each) before the tensor-core products, so a few
-# bf16 ulps of the gradient's scale, 1e-2, is the bound.
-G_REL = 1e-2
+# bf16 ulps of the gradient's scale, 1e-2, bounds the largest error.  Those
+# rounding errors have either sign and most entries are far below the largest
+# (P is nearly one-hot), so the mean error must sit an order of magnitude lower:
+# 1e-3 of the largest oracle gradient.
+G_REL, G_REL_MEAN = 1e-2, 1e-3
 
 
 def check_grads(got, ref, label, relative=False):
@@ -48,6 +51,7 @@ def check_grads(got, ref, label, relative=False):
         if relative:
             scale = max(1.0, float(np.abs(r).max()))
             assert err.max() <= G_REL * scale, f"{label} {name}: max err {err.max():.3g} vs scale {scale:.3g}"
+            assert err.mean() <= G_REL_MEAN * scale, f"{label} {name}: mean err {err.mean():.3g} vs scale {scale:.3g}"
             continue
         assert err.max() <= G_MAX, f"{label} {name}: max err {err.max():.3g} (|ref| max {np.abs(r).max():.3g})"
         assert err.mean() <= G_MEAN, f"{label} {name}: mean err {err.mean():.3g}"
@@ -108,19 +112,26 @@ def test_bwd_dv_closed_form_uniform():
     assert np.all(dk == 0)
 
 
-def test_bwd_full_size_workload_sampled_heads():
+def test_bwd_full_size_workload_eight_heads():
     """The forward + backward workload (B=4 H=16 N=4096 d=128, causal) in the exact
-    launch configuration the benchmark uses; two whole heads are compared with
-    the oracle, every gradient is checked finite."""
+    launch configuration the benchmark uses.  Eight whole heads -- the first and
+    last, middle heads, and heads of every batch -- are compared with the
+    oracle's gradient element by element (max-abs and mean-abs per gradient over
+    those heads); every gradient is checked finite."""
     w = WORKLOADS["bf16_causal_fwdbwd_B4_H16_N4096_d128"]
     pr = make_workload(w)
     dq, dk, dv = run_fwd_bwd(pr, w.causal)
     for t in (dq, dk, dv):
         assert np.all(np.isfinite(t))
-    for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
+    heads = [(0, 0), (0, 7), (1, 3), (1, 12), (2, 8), (2, 15), (3, 5), (w.B - 1, w.H - 1)]
+    got, ref = ([], [], []), ([], [], [])
+    for (b, h) in heads:
         sl = (slice(b, b + 1), slice(h, h + 1))
-        ref = oracle.attention_bwd(pr["q"][sl], pr["k"][sl], pr["v"][sl], pr["do"][sl], pr["scale"], causal=True)
-        check_grads((dq[sl], dk[sl], dv[sl]), ref, f"{w.name} head ({b},{h})")
+        r = oracle.attention_bwd(pr["q"][sl], pr["k"][sl], pr["v"][sl], pr["do"][sl], pr["scale"], causal=True)
+        for i, (g, rr) in enumerate(zip((dq[sl], dk[sl], dv[sl]), r)):
+            got[i].append(g)
+            ref[i].append(rr)
+    check_grads([np.concatenate(x) for x in got], [np.concatenate(x) for x in ref], f"{w.name} heads {heads}")
 
 
 def test_bwd_repeatable():
@@ -140,3 +151,27 @@ def test_bwd_strictly_causal(N):
     (dq, dk, dv), _ = bwd_parity(2, 2, N, 2, seed=N + 7)
     assert np.all(dq[:, :, 0] == 0)
     assert np.all(dk[:, :, N - 1] == 0) and np.all(dv[:, :, N - 1] == 0)
+
+
+def test_bwd_starved_pipeline_times_out_and_recovers():
+    """The test hook makes the backward producer stop after its first Q / dO
+    tile: every bounded wait downstream gives up, the launch reports
+    FA_ERR_TIMEOUT (the CTA drains its copies and products and frees its tensor
+    memory), and the next normal call is correct again."""
+    m = fa()
+    pr = make_problem(1, 2, 512, 128, "bf16", seed=15, backward=True)
+    q, k, v, do = (pr[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = m.attention_fwd(q, k, v, pr["scale"], causal=False)
+    m.fa_check_device_error()
+    m.fa_set_wait_timeout_ms(50)
+    m.fa_debug_inject(2)
+    try:
+        m.attention_bwd(q, k, v, o, lse, do, pr["scale"], causal=False)
+        with pytest.raises(m.FaError) as ei:
+            m.fa_check_device_error()
+        assert ei.value.status == m.FA_ERR_TIMEOUT
+    finally:
+        m.fa_debug_inject(0)
+        m.fa_set_wait_timeout_ms(1000)
+    m.fa_check_device_error()  # the status word was cleared
+    bwd_parity(1, 2, 512, causal=False, seed=15)

@@ -5,9 +5,10 @@ inside an allocator's own hooks, runtimes whose device pool is fixed and fully
 handed out at start-up, and hosts that forbid allocation after initialisation.
 fa_bwd_noalloc serves them with a fixed device array inside the library instead
 of a caller workspace.  These tests check that it gives the same gradients as
-fa_bwd with a workspace, on two calls in a row (the second call finds the first
-call's data still in the shared array), and that a problem too large for the
-fixed array is refused with a clear error.
+fa_bwd with a workspace, and that both match the float64 oracle, on two calls in
+a row (the second call finds the first call's data still in the shared array),
+and that a problem too large for the fixed array is refused with a clear
+error.
 
 This file is named so that pytest collects it last.
 """
@@ -18,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from online_softmax_14_b300 import _binding as B
 from online_softmax_14_b300.inputs import make_problem
 
@@ -44,10 +46,13 @@ def test_noalloc_matches_workspace_backward_twice():
     for (Bs, H, N), causal, seed in cases:
         pr = make_problem(Bs, H, N, 128, "bf16", seed=seed, backward=True)
         got, ref = _grads_both_ways(pr, causal)
-        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        exact = oracle.attention_bwd(pr["q"], pr["k"], pr["v"], pr["do"], pr["scale"], causal=causal)
+        for name, g, r, x in zip(("dQ", "dK", "dV"), got, ref, exact):
             assert np.all(np.isfinite(g)), f"{name} (N={N}): non-finite"
-            err = np.abs(g - r)
-            assert err.max() <= G_MAX and err.mean() <= G_MEAN, f"{name} (N={N}): max err {err.max():.3g}"
+            for other, label in ((r, "fa_bwd"), (x, "oracle")):
+                err = np.abs(g - other)
+                assert err.max() <= G_MAX and err.mean() <= G_MEAN, \
+                    f"{name} (N={N}) vs {label}: max err {err.max():.3g}, mean {err.mean():.3g}"
 
 
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
