@@ -17,7 +17,13 @@ carries:
   * clocks    -- SM clocks and throttle reasons sampled during the timed region;
   * fwd_bwd   -- forward and backward (recompute) TFLOP/s of the training
                  workload, bf16 causal B=4 H=16 N=4096 d=128 (backward FLOPs
-                 10*B*H*N^2*d, halved for causal).
+                 10*B*H*N^2*d, halved for causal);
+  * configs   -- the other forward workloads (float32 B=1 H=1 N=256 d=64; bf16
+                 causal B=4 H=16 N=2048 d=64; the padded x8 stress workload
+                 B=8 H=16 N=1024 d=128), each with its roofline fraction;
+  * standard  -- standard attention (S and P written to device memory in full)
+                 next to the tiled forward on two workloads' shapes;
+  * merge     -- the split-key merge, device-memory bound.
 With --impl reference the float64 oracle itself is timed (rank 0 only).
 Multi-GPU (torchrun): every rank runs its own replica of the workload, no data
 exchange; value = all ranks' FLOPs / the slowest rank's time ("weak" scaling).
@@ -112,7 +118,7 @@ class ClockSampler:
     background thread, through NVML when importable, else an nvidia-smi
     subprocess; only samples taken between mark_start() and mark_end() count."""
 
-    def __init__(self, device_index: int, period_ms: int = 20):
+    def __init__(self, device_index: int, period_ms: int = 5):
         self.period_ms = period_ms
         self.samples = []  # (monotonic time, sm_mhz, reasons bitmask)
         self.max_mhz = None
@@ -198,8 +204,8 @@ class ClockSampler:
         out = {"sm_mhz": statistics.median([s[1] for s in inside]) if inside else None,
                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons), "samples": len(inside),
                "source": "nvml" if self.nv else "nvidia-smi"}
-        if not inside and self.error:
-            out["error"] = self.error
+        if self.error:
+            out["note"] = self.error
         return out
 
 
@@ -261,6 +267,10 @@ def main():
                     help="timed steps of the forward + backward workload (0 skips it)")
     ap.add_argument("--merge-steps", type=int, default=20,
                     help="timed steps of the split-key merge (0 skips it)")
+    ap.add_argument("--config-steps", type=int, default=20,
+                    help="timed steps of each of the other forward workloads (0 skips them)")
+    ap.add_argument("--std-steps", type=int, default=3,
+                    help="timed steps of standard attention on two workloads' shapes (0 skips it)")
     ap.add_argument("--bwd-shape", default=None,
                     help="B,H,N: a custom causal d=128 forward + backward workload (profiling runs)")
     args = ap.parse_args()
@@ -365,6 +375,10 @@ def main():
         line["fwd_bwd"] = run_fwd_bwd(args, fa, dev, stream, dist)
     if args.merge_steps > 0 and not args.shape:
         line["merge"] = run_merge(args, fa, w, dev, stream, peaks)
+    if args.config_steps > 0 and not args.shape:
+        line["configs"] = run_configs(args, fa, dev, stream, peaks)
+    if args.std_steps > 0 and not args.shape:
+        line["standard"] = run_standard(args, fa, dev, stream, peaks)
     if rank == 0 and world == 1 and args.cpu_budget_s > 0:
         line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_budget_s)
     if rank == 0:
@@ -421,6 +435,105 @@ def run_fwd_bwd(args, fa, dev, stream, dist):
             "fwd_bwd_tflops": round((ff + fb) / (ms_f + ms_b) / 1e9, 2),
             "flops": {"fwd": ff, "bwd": fb, "bwd_formula": "10*B*H*N^2*d, halved for causal"},
             "gpu_launches_per_bwd": 2}
+
+
+FP32_FFMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # 148 SMs x 128 FP32 lanes x 2 FLOP (FMA) x 2.032 GHz
+
+
+def _time(fn, steps, warmup, stream):
+    for _ in range(max(3, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_configs(args, fa, dev, stream, peaks):
+    """The other forward workloads, each timed over --config-steps launches with
+    CUDA events on the launching stream, with its roofline fraction: the bf16
+    ones against the measured dense-bf16 peak; the float32 one (CUDA cores)
+    against the FP32 FMA rate of 148 SMs x 128 lanes x 2 FLOP at 2.032 GHz.  The
+    padded stress workload reports the formula FLOPs (4*B*H*N^2*d) and the
+    effective ones (4*H*d*N*sum(kv_len), the keys actually visible)."""
+    out = {}
+    peak = float(peaks["bf16_tflops"])
+    for name in ("fp32_B1_H1_N256_d64", "bf16_causal_B4_H16_N2048_d64", "bf16_padded_stress_B8_H16_N1024_d128"):
+        w = WORKLOADS[name]
+        inp = make_workload(w, seed=args.seed)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        kv = None if inp["kv_len"] is None else inp["kv_len"].to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        dt = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP32
+
+        def step():
+            fa.fa_fwd_ex(dt, q, k, v, o, lse, kv, w.B, w.H, w.N, w.d, inp["scale"], w.causal, stream)
+
+        ms = _time(step, args.config_steps, args.warmup, stream)
+        fa.fa_check_device_error(stream)
+        f = flops_per_step(w)
+        tf = f / ms / 1e9
+        r = {"ms": round(ms, 5), "tflops": round(tf, 2), "dtype": w.dtype}
+        if w.dtype == "bf16":
+            r["roofline"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(tf / peak, 4), "peak_source": "measured bf16_tflops (burst)"}
+        else:
+            r["roofline"] = {"bound": "alu", "achieved": round(tf, 3), "peak": round(FP32_FFMA_TFLOPS, 1),
+                             "unit": "TFLOP/s", "frac": round(tf / FP32_FFMA_TFLOPS, 5),
+                             "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz"}
+        if w.padded:
+            eff = 4.0 * w.H * w.d * w.N * float(inp["kv_len"].sum())
+            r["effective_tflops"] = round(eff / ms / 1e9, 2)
+            r["effective_frac"] = round(eff / ms / 1e9 / peak, 4)
+            r["flops"] = {"formula": f, "effective": eff, "note": "effective counts only keys < kv_len[b]"}
+        out[name] = r
+    return out
+
+
+def run_standard(args, fa, dev, stream, peaks):
+    """Standard attention (fa_std_fwd: S = scale Q K^T written in full as float32,
+    P = softmax(S) written as bf16, then O = P V) next to the tiled forward on
+    the same inputs, for two workloads' shapes: time of each, the algorithmic
+    device-memory bytes of each, and the share of the standard path's bytes that
+    are the N x N matrices (the HBM-traffic exercise of the Exercises page)."""
+    out = {}
+    hbm = float(peaks.get("hbm_gbs", 6400.0))
+    for name in ("bf16_causal_B4_H16_N2048_d64", "bf16_causal_B2_H32_N8192_d128"):
+        w = WORKLOADS[name]
+        inp = make_workload(w, seed=args.seed)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        nbytes = fa.fa_std_workspace_size(w.B, w.H, w.N)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def std():
+            fa.fa_std_fwd(q, k, v, o, lse, None, ws, nbytes, w.B, w.H, w.N, w.d, inp["scale"], w.causal, stream)
+
+        def tiled():
+            fa.fa_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, inp["scale"], w.causal, stream)
+
+        ms_std = _time(std, args.std_steps, 3, stream)
+        ms_tiled = _time(tiled, max(args.std_steps, 10), 3, stream)
+        fa.fa_check_device_error(stream)
+        bh, n, d = w.B * w.H, w.N, w.d
+        io = 4 * bh * n * d * 2 + bh * n * 4           # Q, K, V read; O written; lse written
+        quad = bh * n * n * (4 + 4 + 2 + 2)             # S written and read (f32), P written and read (bf16)
+        out[name] = {"ms_standard": round(ms_std, 4), "ms_tiled": round(ms_tiled, 4),
+                     "speedup_tiled_over_standard": round(ms_std / ms_tiled, 2),
+                     "bytes_standard": io + quad, "bytes_tiled": io,
+                     "nxn_share_of_standard_bytes": round(quad / (io + quad), 5),
+                     "standard_gbs": round((io + quad) / (ms_std * 1e-3) / 1e9, 1),
+                     "standard_hbm_frac": round((io + quad) / (ms_std * 1e-3) / 1e9 / hbm, 4),
+                     "workspace_bytes": nbytes, "launches_standard": 3, "launches_tiled": 1}
+        del ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_merge(args, fa, w, dev, stream, peaks, n_parts=4):

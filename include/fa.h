@@ -208,6 +208,24 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const float* lse, float* dq, float* dk, float* dv, int B, int H, int N, int d, float scale,
                          int causal, void* stream);
 
+/*
+ * fa_std_fwd -- standard attention, the comparator the tiled method is measured
+ * against ("Foundations -- Flash attention and efficient attention", section 10;
+ * "Exercises", the memory-size and HBM-traffic exercises): the N x N score
+ * matrix S = scale * Q K^T is written to device memory in full (float32), then
+ * P = softmax_rows(S) (bf16, masked entries 0), then O = P V and lse.  Same
+ * inputs, outputs, masks (causal 0 / 1 / 2, kv_len) and conventions as
+ * fa_fwd_ex with FA_BF16; d = 64 or 128.  Not the fast path: it exists to
+ * measure what keeping S and P on chip saves.
+ *   workspace : device memory of at least fa_std_workspace_size(B, H, N) bytes,
+ *               16-byte aligned, owned by the caller (S and P live there).
+ * The products run on the tensor cores (tcgen05), the softmax on the CUDA cores.
+ */
+size_t fa_std_workspace_size(int B, int H, int N);
+fa_status fa_std_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len,
+                     void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                     void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* fa_status_string(int status);
 

@@ -60,6 +60,10 @@ _lib.fa_merge.restype = _i
 _lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
 _lib.fa_bwd_noalloc.restype = _i
 FA_BWD_NOALLOC_MAX_ROWS = 524288
+_lib.fa_std_workspace_size.argtypes = [_i, _i, _i]
+_lib.fa_std_workspace_size.restype = _sz
+_lib.fa_std_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _vp]
+_lib.fa_std_fwd.restype = _i
 
 
 class FaError(RuntimeError):
@@ -257,3 +261,30 @@ def attention_bwd(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, st
     fa_bwd_qk(q, k, v, o, do, lse.contiguous(), kv_len, dq, dk, dv, ws, ws_bytes, B, H, Nq, Nk, d, scale, causal,
               stream)
     return dq, dk, dv
+
+
+def fa_std_workspace_size(B, H, N) -> int:
+    return int(_lib.fa_std_workspace_size(B, H, N))
+
+
+def fa_std_fwd(q, k, v, o, lse, kv_len, workspace, workspace_bytes, B, H, N, d, scale, causal, stream=None) -> None:
+    _check(_lib.fa_std_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(kv_len), _ptr(workspace),
+                           int(workspace_bytes), B, H, N, d, float(scale), _causal(causal), _stream(stream)))
+
+
+def standard_attention_fwd(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
+    """O, lse by standard attention (S and P written to device memory in full):
+    the comparator of the tiled kernels.  q, k, v bf16 [B, H, N, d] CUDA tensors.
+    Allocates the outputs and the S / P workspace with PyTorch, then runs
+    ``fa_std_fwd``."""
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    nbytes = fa_std_workspace_size(B, H, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    fa_std_fwd(q, k, v, o, lse, kv_len, ws, nbytes, B, H, N, d, scale, causal, stream)
+    return o, lse

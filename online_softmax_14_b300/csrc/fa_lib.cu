@@ -6,8 +6,14 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <map>
+#include <memory>
+#include <queue>
+#include <tuple>
+#include <vector>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -19,6 +25,7 @@
 #include "fwd_tc.cuh"
 #include "bwd_tc.cuh"
 #include "merge.cuh"
+#include "std_attn.cuh"
 
 namespace fa {
 // Status word of the current device: kernels OR their timeout codes into it;
@@ -37,6 +44,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kSlotsD128 = 4;  // K/V ring slots of the forward (32 KB each at d = 128)
 constexpr int kSlotsD64 = 8;   // (16 KB each at d = 64)
 constexpr int kStagesBwd = 2;
+constexpr int kStagesStdS = 2;   // standard attention, S = Q K^T: K = d fits in two 64-element chunks
+constexpr int kStagesStdO = 3;   // standard attention, O = P V: K = Nk streams through three stages
 
 thread_local char t_err[512] = "";
 std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};
@@ -58,6 +67,7 @@ struct DeviceState {
   bool ready = false;
   unsigned long long ctx_id = 0;   // the CUDA context the fields below belong to
   int cc_major = 0, cc_minor = 0;
+  int sm_count = 0;
   unsigned int* status = nullptr;  // device address of fa::g_status_word
   unsigned int* taken = nullptr;   // device address of fa::g_status_taken
 };
@@ -116,6 +126,8 @@ fa_status device_state(DeviceState** out) {
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if ((e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
     if (s.cc_major != 10 || s.cc_minor != 3)
       return fail(FA_ERR_UNSUPPORTED, "libfa is built for sm_103a; device %d is sm_%d%d", dev, s.cc_major,
                   s.cc_minor);
@@ -137,6 +149,14 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fa::BwdLayout<kStagesBwd>::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+    if ((e = cudaFuncSetAttribute(fa::std_gemm_kernel<kStagesStdS, false, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  fa::StdGemmLayout<kStagesStdS>::BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(standard S)");
+    if ((e = cudaFuncSetAttribute(fa::std_gemm_kernel<kStagesStdO, true, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  fa::StdGemmLayout<kStagesStdO>::BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(standard O)");
     s.ctx_id = ctx_id;
     s.ready = true;
   }
@@ -166,6 +186,23 @@ fa_status make_map(CUtensorMap* m, const void* base, int d, int N, int BH, const
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return FA_OK;
+}
+
+// [BH, rows, cols] bf16 with row stride `ld` elements (ld * 2 a multiple of 16),
+// 64 x 128 x 1 boxes with 128-byte swizzle; columns past `cols` read as zero.
+fa_status make_map_strided(CUtensorMap* m, const void* base, int cols, int rows, int BH, long long ld,
+                           const char* name) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(rows) * ld * 2};
+  cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -218,6 +255,74 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
   return FA_OK;
 }
 
+// Work list of a persistent forward launch (see fa::FwdSched), built on the
+// host once per problem shape.  Items are weighted by the key tiles their two
+// query tiles process, plus two for the item's fixed costs; the kv_len values
+// live on the device and are not looked at (a padded problem just balances
+// less well).  Heads are taken in groups whose K and V fit in about 48 MB, so
+// that the CTAs working at one time share them in L2; within a group the items
+// go heaviest first, each to the CTA with the least work so far.
+struct SchedKey {
+  int BH, N, Nk, causal, qoff, D, G;
+  bool operator<(const SchedKey& o) const {
+    return std::tie(BH, N, Nk, causal, qoff, D, G) < std::tie(o.BH, o.N, o.Nk, o.causal, o.qoff, o.D, o.G);
+  }
+};
+std::map<SchedKey, std::unique_ptr<fa::FwdSched>> g_sched;
+std::mutex g_sched_mu;
+
+const fa::FwdSched* fwd_schedule(int BH, int N, int Nk, int causal, int qoff, int D, int G) {
+  const SchedKey key{BH, N, Nk, causal, qoff, D, G};
+  std::lock_guard<std::mutex> lk(g_sched_mu);
+  auto found = g_sched.find(key);
+  if (found != g_sched.end()) return found->second.get();
+  auto sc = std::make_unique<fa::FwdSched>();
+  const int n_qt = (N + 127) / 128, n_pair = (n_qt + 1) / 2;
+  const long long n_items = static_cast<long long>(BH) * n_pair;
+  sc->n_items = static_cast<int>(n_items);
+  sc->table = 0;
+  if (n_items <= fa::FWD_SCHED_MAX_ITEMS && G <= fa::FWD_SCHED_MAX_CTAS) {
+    const int n_kv_all = (Nk + 127) / 128;
+    auto tiles = [&](int qt) -> int {  // as the kernel computes it, without kv_len
+      if (qt >= n_qt) return 0;
+      if (!causal) return n_kv_all;
+      const int last_key = std::min(qt * 128 + 128, N) - 1 + qoff - 1;
+      return last_key < 0 ? 0 : std::min(n_kv_all, last_key / 128 + 1);
+    };
+    std::vector<int> w(n_pair);
+    for (int pr = 0; pr < n_pair; ++pr) w[pr] = tiles(2 * pr) + tiles(2 * pr + 1) + 2;
+    const double kv_head = 2.0 * Nk * D * 2;
+    const int hpg = std::max(1, static_cast<int>(48.0 * 1024 * 1024 / kv_head));
+    std::vector<std::vector<uint32_t>> lists(G);
+    using Load = std::pair<long long, int>;  // (work so far, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < G; ++c) heap.push({0, c});
+    std::vector<std::pair<int, uint32_t>> group;  // (weight, item id)
+    for (int g0 = 0; g0 < BH; g0 += hpg) {
+      group.clear();
+      for (int bh = g0; bh < std::min(BH, g0 + hpg); ++bh)
+        for (int pr = n_pair - 1; pr >= 0; --pr) group.push_back({w[pr], static_cast<uint32_t>(bh * n_pair + pr)});
+      std::stable_sort(group.begin(), group.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+      for (const auto& it : group) {
+        Load ld = heap.top();
+        heap.pop();
+        lists[ld.second].push_back(it.second);
+        heap.push({ld.first + it.first, ld.second});
+      }
+    }
+    int pos = 0;
+    for (int c = 0; c < G; ++c) {
+      sc->start[c] = static_cast<uint16_t>(pos);
+      for (uint32_t id : lists[c]) sc->list[pos++] = id;
+    }
+    sc->start[G] = static_cast<uint16_t>(pos);
+    sc->table = 1;
+  }
+  const fa::FwdSched* out = sc.get();
+  g_sched[key] = std::move(sc);
+  return out;
+}
+
 template <int D, int STAGES>
 fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len, int B,
                     int H, int N, int Nk, float scale, int causal, cudaStream_t stream, const DeviceState& ds) {
@@ -243,9 +348,13 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.load();
-  const long long blocks = static_cast<long long>((p.n_qt + 1) / 2) * BH;  // two query tiles per CTA
-  if (blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
-  fa::fwd_bf16_tc_kernel<D, STAGES><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, p);
+  // persistent grid: one CTA per SM (each holds all of an SM's tensor memory),
+  // fewer when there are fewer items
+  const long long n_items = static_cast<long long>((p.n_qt + 1) / 2) * BH;
+  if (n_items > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "problem too large");
+  const int G = static_cast<int>(std::min<long long>(std::max(1, ds.sm_count), n_items));
+  const fa::FwdSched* sc = fwd_schedule(BH, N, Nk, causal, p.qoff, D, G);
+  fa::fwd_bf16_tc_kernel<D, STAGES><<<static_cast<unsigned>(G), 384, L::BYTES, stream>>>(mq, mk, mv, p, *sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc_kernel");
   return FA_OK;
@@ -327,6 +436,80 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.inject = g_inject.load();
   fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_bf16_tc_kernel");
+  return FA_OK;
+}
+
+
+// Standard attention's workspace: S (float32) and P (bf16), each [BH][Nq][ld]
+// with ld = Nk rounded up to 64 (rows of P 128-byte aligned for the tensor map).
+long long std_ld(int Nk) { return (static_cast<long long>(Nk) + 63) / 64 * 64; }
+size_t std_ws_bytes(int B, int H, int Nq, int Nk) {
+  return static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(Nq) * static_cast<size_t>(std_ld(Nk)) * 6;
+}
+
+fa_status launch_std(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len,
+                     void* ws, int B, int H, int N, int Nk, int d, float scale, int causal, cudaStream_t stream,
+                     const DeviceState& ds) {
+  const int BH = B * H;
+  const long long ld = std_ld(Nk);
+  float* s_buf = static_cast<float*>(ws);
+  __nv_bfloat16* p_buf = reinterpret_cast<__nv_bfloat16*>(s_buf + static_cast<size_t>(BH) * N * ld);
+  CUtensorMap mq, mk, mp, mv;
+  fa_status s;
+  if ((s = make_map(&mq, q, d, N, BH, "q")) != FA_OK) return s;
+  if ((s = make_map(&mk, k, d, Nk, BH, "k")) != FA_OK) return s;
+  if ((s = make_map_strided(&mp, p_buf, Nk, N, BH, ld, "p")) != FA_OK) return s;
+  if ((s = make_map(&mv, v, d, Nk, BH, "v", 64)) != FA_OK) return s;
+  const long long tiles_m = (N + 127) / 128, tiles_n = (Nk + 127) / 128;
+  if (tiles_m * tiles_n > 0x7fffffffll || BH > 65535) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  // S = scale Q K^T, every entry
+  fa::StdGemmParams gs{};
+  gs.c = s_buf;
+  gs.ldc = ld;
+  gs.c_batch = static_cast<long long>(N) * ld;
+  gs.M = N;
+  gs.N = Nk;
+  gs.K = d;
+  gs.tiles_n = static_cast<int>(tiles_n);
+  gs.alpha = scale;
+  gs.status = ds.status;
+  gs.timeout_ns = g_timeout_ns.load();
+  fa::std_gemm_kernel<kStagesStdS, false, true>
+      <<<dim3(static_cast<unsigned>(tiles_m * tiles_n), BH), 128, fa::StdGemmLayout<kStagesStdS>::BYTES, stream>>>(
+          mq, mk, gs);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch std_gemm_kernel (S)");
+  // P = softmax(S) with the mask, lse
+  fa::StdSoftmaxParams sp{};
+  sp.s = s_buf;
+  sp.p = p_buf;
+  sp.lse = lse;
+  sp.kv_len = kv_len;
+  sp.ld = ld;
+  sp.BH = BH;
+  sp.H = H;
+  sp.Nq = N;
+  sp.Nk = Nk;
+  sp.causal = causal;
+  sp.qoff = causal_qoff(N, Nk, causal);
+  const long long rows = static_cast<long long>(BH) * N;
+  fa::std_softmax_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(sp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch std_softmax_kernel");
+  // O = P V over every key
+  fa::StdGemmParams go{};
+  go.c = o;
+  go.ldc = d;
+  go.c_batch = static_cast<long long>(N) * d;
+  go.M = N;
+  go.N = d;
+  go.K = Nk;
+  go.tiles_n = 1;
+  go.alpha = 1.f;
+  go.status = ds.status;
+  go.timeout_ns = g_timeout_ns.load();
+  fa::std_gemm_kernel<kStagesStdO, true, false>
+      <<<dim3(static_cast<unsigned>(tiles_m), BH), 128, fa::StdGemmLayout<kStagesStdO>::BYTES, stream>>>(mp, mv, go);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch std_gemm_kernel (O)");
   return FA_OK;
 }
 
@@ -492,6 +675,29 @@ fa_status fa_merge(int dtype, const void* o_parts, const float* lse_parts, int n
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_kernel");
   return FA_OK;
+}
+
+size_t fa_std_workspace_size(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return std_ws_bytes(B, H, N, N);
+}
+
+fa_status fa_std_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* kv_len,
+                     void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                     void* stream) {
+  t_err[0] = '\0';
+  fa_status s;
+  if ((s = check_causal(causal)) != FA_OK) return s;
+  if ((s = check_common(q, k, v, o, lse, B, H, N, d, scale, 16)) != FA_OK) return s;
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "standard attention serves d = 64 or 128 (got %d)", d);
+  if (!workspace || !aligned(workspace, 16)) return fail(FA_ERR_INVALID, "workspace must be a 16-byte aligned device pointer");
+  const size_t need = std_ws_bytes(B, H, N, N);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes, need);
+  DeviceState* ds = nullptr;
+  if ((s = device_state(&ds)) != FA_OK) return s;
+  return launch_std(q, k, v, o, lse, kv_len, workspace, B, H, N, N, d, scale, causal,
+                    static_cast<cudaStream_t>(stream), *ds);
 }
 
 const char* fa_status_string(int status) {

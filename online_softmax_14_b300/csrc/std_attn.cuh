@@ -111,13 +111,9 @@ __global__ void __launch_bounds__(128)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
     constexpr uint32_t IDESC = idesc_bf16_f32(128, 128, B_MN);
-    bool ok = true;
     for (int c = 0; c < n_k; ++c) {
       const int s = c % STAGES;
-      if (!mbar_wait_w(full + 8 * s, (c / STAGES) & 1, wc, ST_STD_TIMEOUT)) {
-        ok = false;
-        break;
-      }
+      if (!mbar_wait_w(full + 8 * s, (c / STAGES) & 1, wc, ST_STD_TIMEOUT)) break;
       tc_fence_after();
       const uint32_t a = sbase + s * L::STAGE, b = a + L::A_BYTES;
 #pragma unroll
@@ -130,10 +126,9 @@ __global__ void __launch_bounds__(128)
       }
       umma_commit_w(empty + 8 * s);
     }
-    if (ok) umma_commit_w(acc_full);
-    if (!ok) {
-      umma_commit_w(acc_full);  // let the epilogue drain what was issued
-    }
+    // also after a failed wait: the epilogue then finds the abort flag set and
+    // only drains what was issued
+    umma_commit_w(acc_full);
   }
 
   // --------------------------------------------------------------- epilogue --
@@ -191,6 +186,8 @@ __global__ void __launch_bounds__(128)
     if (!drained) atomicOr(p.status, ST_DRAIN);
   }
   if (warp == 1) {
+    // nothing may be in flight on the tensor cores when the CTA frees TMEM
+    if (!mbar_wait_drain(acc_full, 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
     tc_fence_after();
     tmem_dealloc(tmem, 128);
   }
