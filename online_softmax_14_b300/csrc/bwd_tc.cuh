@@ -68,6 +68,7 @@
 #pragma once
 #include "exp2_poly.cuh"
 #include "ptx.cuh"
+#include "worklist.cuh"
 
 // Every FA_BWD_EXP2_FMA_EVERY-th pair of probabilities takes its exponentials on
 // the FMA pipe (exp2_fma2) instead of the special-function unit; 0 = none.
@@ -195,10 +196,10 @@ struct BwdLayout {
   static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: nl[128], nd[128]
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
   // barriers: kv_full, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full, dp_full,
-  //           ds_full, dq_full, dq_empty, red_ready[2], dkv_done, drain
-  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 2 + 2;
+  //           ds_full, dq_full, dq_empty, red_ready[2], dkv_done, drain, q_issued, kv_free
+  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 2 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int USED = OFF_MISC + 16;
+  static constexpr int USED = OFF_MISC + 32;
   static constexpr int BYTES = 232448;             // the whole per-CTA budget
   static constexpr int SLACK = BYTES - USED;        // room to align the base up to 1024 bytes
   // S^T, then P^T (bf16, in each half's own columns), | dP^T, then dQ^T | dV | dK
@@ -230,29 +231,29 @@ struct BwdSmem {
   __device__ __forceinline__ uint32_t red_ready(int h) const { return bar(7 + 4 * STAGES + h); }
   __device__ __forceinline__ uint32_t dkv_done() const { return bar(9 + 4 * STAGES); }
   __device__ __forceinline__ uint32_t drain() const { return bar(10 + 4 * STAGES); }
+  // the producer has issued the load of Q_t (one phase per query tile)
+  __device__ __forceinline__ uint32_t q_issued() const { return bar(11 + 4 * STAGES); }
+  // every product of an item that reads K or V has run (one phase per item)
+  __device__ __forceinline__ uint32_t kv_free() const { return bar(12 + 4 * STAGES); }
 };
 
-// Where a backward CTA works: its (batch, head), key tile and the range of query
-// tiles that see it.  Each role computes this inside its own branch (from a
-// volatile read of the CTA index, so the copies are not merged into one value
-// computed before the branch): nothing then stays live across the role's
-// register-budget change.
-struct BwdTile {
+// One backward work item: a 128-key tile of one (batch, head), and the range of
+// query tiles that see it (under a causal mask, from the tile holding the key
+// tile's first visible query on).  Each role computes it alike.
+struct BwdItem {
   int bh, k0, kv_limit, i0, n_it;
 };
 template <int BN, int BM, typename Params>
-__device__ __forceinline__ BwdTile bwd_tile(const Params& p) {
-  uint32_t cta;
-  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(cta));
-  BwdTile g;
-  // head-major; within a head the key tiles with the most query tiles first
-  g.bh = static_cast<int>(cta) / p.n_kt;
-  g.k0 = (static_cast<int>(cta) % p.n_kt) * BN;
+__device__ __forceinline__ BwdItem bwd_item(const Params& p, const WorkList& w, int k) {
+  int bh, kt;  // units of a head: its key tiles, the first one heaviest under a causal mask
+  wl_item(w, k, p.n_kt, false, bh, kt);
+  BwdItem g;
+  g.bh = bh;
+  g.k0 = kt * BN;
   g.kv_limit = p.Nk;
-  if (p.kv_len) g.kv_limit = min(p.Nk, max(0, p.kv_len[g.bh / p.H]));
+  if (p.kv_len) g.kv_limit = min(p.Nk, max(0, p.kv_len[bh / p.H]));
   const int n_qt = (p.N + BM - 1) / BM;
-  // first query tile that sees a key of this tile: causal, key k0 is visible to
-  // query rows i >= k0 - qoff + 1
+  // causal: key k0 is visible to query rows i >= k0 - qoff + 1
   g.i0 = p.causal ? max(0, g.k0 - p.qoff + 1) / BM : 0;
   g.n_it = (g.k0 < g.kv_limit && g.i0 < n_qt) ? n_qt - g.i0 : 0;
   return g;
@@ -262,7 +263,8 @@ template <int STAGES>
 __global__ void __launch_bounds__(384, 1)
     bwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p,
+                       const __grid_constant__ WorkList sc) {
   using L = BwdLayout<STAGES>;
   constexpr int D = L::D;
   extern __shared__ uint8_t smem_raw[];
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* issued_q = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
   volatile int* issued_do = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);
+  volatile int* issued_kv = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);  // K/V loads issued
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
@@ -300,9 +303,12 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(sm.red_ready(1), 128);
     mbar_init(sm.dkv_done(), 1);
     mbar_init(sm.drain(), 1);
+    mbar_init(sm.q_issued(), 1);
+    mbar_init(sm.kv_free(), 1);
     *abort_flag = 0;
     *issued_q = 0;
     *issued_do = 0;
+    *issued_kv = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -325,117 +331,155 @@ __global__ void __launch_bounds__(384, 1)
     reg_lower<BWD_REGS_LOW>();
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
     const uint32_t sbase = sm.base;
-    const BwdTile g = bwd_tile<L::BN, L::BM>(p);
-    const int bh = g.bh, k0 = g.k0, i0 = g.i0, n_it = g.n_it;
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
     // ------------------------------------------------------------ producer --
-    if (lane == 0 && n_it > 0) {
-      mbar_arrive_expect_tx(sm.kv_full(), 2 * L::TILE);
+    // Per item: K and V (once the previous item's last products reading them
+    // have run), then Q_t + nl_t + nd_t and dO_t of every query tile through the
+    // ring.  T counts query tiles over all of the CTA's items (ring slot and
+    // barrier phases).
+    if (lane == 0) {
+      int T = 0, ni = 0;
+      bool go = true;
+      for (int k = 0; go && k < n_items; ++k) {
+        const BwdItem g = bwd_item<L::BN, L::BM>(p, sc, k);
+        if (g.n_it == 0) continue;
+        if (ni > 0 && !mbar_wait(sm.kv_free(), (ni - 1) & 1, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(sm.kv_full(), 2 * L::TILE);
 #pragma unroll
-      for (int kb = 0; kb < L::KB; ++kb) {
-        tma_load_3d(sbase + L::OFF_K + kb * L::COLBLK, &tm_k, sm.kv_full(), kb * 64, k0, bh);
-        tma_load_3d(sbase + L::OFF_V + kb * L::COLBLK, &tm_v, sm.kv_full(), kb * 64, k0, bh);
-      }
-      for (int t = 0; t < n_it; ++t) {
-        const int st = t % STAGES;
-        const uint32_t eph = ((t / STAGES) - 1) & 1;
-        const int q0 = (i0 + t) * L::BM;
-        if (p.inject == 2 && t == 1) break;  // test hook: starve the consumers after the first tile
-        if (t >= STAGES && !mbar_wait(sm.q_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(sm.q_full(st), L::TILE + 1024);
+        for (int kb = 0; kb < L::KB; ++kb) {
+          tma_load_3d(sbase + L::OFF_K + kb * L::COLBLK, &tm_k, sm.kv_full(), kb * 64, g.k0, g.bh);
+          tma_load_3d(sbase + L::OFF_V + kb * L::COLBLK, &tm_v, sm.kv_full(), kb * 64, g.k0, g.bh);
+        }
+        *issued_kv = ++ni;
+        for (int t = 0; t < g.n_it; ++t, ++T) {
+          const int st = T % STAGES;
+          const uint32_t eph = ((T / STAGES) - 1) & 1;
+          const int q0 = (g.i0 + t) * L::BM;
+          if (p.inject == 2 && T == 1) {  // test hook: starve the consumers after the first tile
+            go = false;
+            break;
+          }
+          if (T >= STAGES && !mbar_wait(sm.q_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) {
+            go = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sm.q_full(st), L::TILE + 1024);
 #pragma unroll
-        for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(sbase + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, sm.q_full(st), kb * 64, q0, bh);
-        // nl and nd of the tile's 128 queries (rows padded to a multiple of 128)
-        const size_t ws = static_cast<size_t>(bh) * p.Np + q0;
-        bulk_load(sbase + L::OFF_STAT + st * 1024, p.nl + ws, 512, sm.q_full(st));
-        bulk_load(sbase + L::OFF_STAT + st * 1024 + 512, p.nd + ws, 512, sm.q_full(st));
-        *issued_q = t + 1;
-        if (t >= STAGES && !mbar_wait(sm.do_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(sm.do_full(st), L::TILE);
+          for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(sbase + L::OFF_Q + st * L::TILE + kb * L::COLBLK, &tm_q, sm.q_full(st), kb * 64, q0, g.bh);
+          // nl and nd of the tile's 128 queries (rows padded to a multiple of 128)
+          const size_t ws = static_cast<size_t>(g.bh) * p.Np + q0;
+          bulk_load(sbase + L::OFF_STAT + st * 1024, p.nl + ws, 512, sm.q_full(st));
+          bulk_load(sbase + L::OFF_STAT + st * 1024 + 512, p.nd + ws, 512, sm.q_full(st));
+          *issued_q = T + 1;
+          mbar_arrive(sm.q_issued());
+          if (T >= STAGES && !mbar_wait(sm.do_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) {
+            go = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sm.do_full(st), L::TILE);
 #pragma unroll
-        for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(sbase + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, sm.do_full(st), kb * 64, q0, bh);
-        *issued_do = t + 1;
+          for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(sbase + L::OFF_DO + st * L::TILE + kb * L::COLBLK, &tm_do, sm.do_full(st), kb * 64, q0, g.bh);
+          *issued_do = T + 1;
+        }
       }
     }
     tc_fence_before();
     cta_bar_sync<384>();
-    if (lane == 0 && n_it > 0 && *abort_flag) {
+    if (lane == 0 && *abort_flag) {
       // an aborted CTA may not exit while copies it issued are still landing
-      bool ok = mbar_wait_drain(sm.kv_full(), 0, DRAIN_NS);
-      const int nq = *issued_q, nd = *issued_do;
+      const int nk = *issued_kv, nq = *issued_q, nd = *issued_do;
+      bool drained = nk == 0 || mbar_wait_drain(sm.kv_full(), (nk - 1) & 1, DRAIN_NS);
       for (int t = max(0, nq - STAGES); t < nq; ++t)
-        ok &= mbar_wait_drain(sm.q_full(t % STAGES), (t / STAGES) & 1, DRAIN_NS);
+        drained &= mbar_wait_drain(sm.q_full(t % STAGES), (t / STAGES) & 1, DRAIN_NS);
       for (int t = max(0, nd - STAGES); t < nd; ++t)
-        ok &= mbar_wait_drain(sm.do_full(t % STAGES), (t / STAGES) & 1, DRAIN_NS);
-      if (!ok) atomicOr(p.status, ST_DRAIN);
+        drained &= mbar_wait_drain(sm.do_full(t % STAGES), (t / STAGES) & 1, DRAIN_NS);
+      if (!drained) atomicOr(p.status, ST_DRAIN);
     }
   } else if (warp == 1) {
     reg_lower<BWD_REGS_LOW>();
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
     const uint32_t sbase = sm.base;
-    const int n_it = bwd_tile<L::BN, L::BM>(p).n_it;
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ---------------------------------------------------------- MMA issuer --
     // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
-    if (n_it > 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, L::BM, false, false);  // K Q^T, V dO^T
-      constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, true, false);       // P^T dO, dS^T Q
-      constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, L::BM, true, true);      // K^T dS
-      // Descriptors of the operand bases; an operand at byte offset `off` from a
-      // base is that descriptor plus off >> 4 (the start-address field is the
-      // low 14 bits and every shared address here is below 2^18, so no carry).
-      const uint64_t d_k = sdesc_sw128(sbase + L::OFF_K, 16, 1024);        // K-major: K, V, Q, dO, dS^T
-      const uint64_t d_v = sdesc_sw128(sbase + L::OFF_V, 16, 1024);
-      const uint64_t d_q = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
-      const uint64_t d_do = sdesc_sw128(sbase + L::OFF_DO, 16, 1024);
-      const uint64_t d_ds = sdesc_sw128(sbase + L::OFF_DS, 16, 1024);
-      const uint64_t m_k = sdesc_sw128(sbase + L::OFF_K, L::COLBLK, 1024);  // MN-major: K, Q, dO, dS
-      const uint64_t m_q = sdesc_sw128(sbase + L::OFF_Q, L::COLBLK, 1024);
-      const uint64_t m_do = sdesc_sw128(sbase + L::OFF_DO, L::COLBLK, 1024);
-      const uint64_t m_ds = sdesc_sw128(sbase + L::OFF_DS, L::COLBLK, 1024);
-      constexpr uint32_t TILE16 = L::TILE >> 4;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, L::BM, false, false);  // K Q^T, V dO^T
+    constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, true, false);       // P^T dO, dS^T Q
+    constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, L::BM, true, true);      // K^T dS
+    // Descriptors of the operand bases; an operand at byte offset `off` from a
+    // base is that descriptor plus off >> 4 (the start-address field is the
+    // low 14 bits and every shared address here is below 2^18, so no carry).
+    const uint64_t d_k = sdesc_sw128(sbase + L::OFF_K, 16, 1024);        // K-major: K, V, Q, dO
+    const uint64_t d_v = sdesc_sw128(sbase + L::OFF_V, 16, 1024);
+    const uint64_t d_q = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+    const uint64_t d_do = sdesc_sw128(sbase + L::OFF_DO, 16, 1024);
+    const uint64_t m_k = sdesc_sw128(sbase + L::OFF_K, L::COLBLK, 1024);  // MN-major: K, Q, dO, dS
+    const uint64_t m_q = sdesc_sw128(sbase + L::OFF_Q, L::COLBLK, 1024);
+    const uint64_t m_do = sdesc_sw128(sbase + L::OFF_DO, L::COLBLK, 1024);
+    const uint64_t m_ds = sdesc_sw128(sbase + L::OFF_DS, L::COLBLK, 1024);
+    constexpr uint32_t TILE16 = L::TILE >> 4;
 
-      // S^T = K Q_t^T or dP^T = V dO_t^T: both operands K-major, two column blocks each
-      auto mma_scores = [&](uint32_t d_tm, uint64_t a, uint64_t b) {
+    // S^T = K Q_t^T or dP^T = V dO_t^T: both operands K-major, two column blocks each
+    auto mma_scores = [&](uint32_t d_tm, uint64_t a, uint64_t b) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
-          umma_ss_w(d_tm, a + off, b + off, IDESC_S, kk > 0 ? 1u : 0u);
-        }
-      };
-      // Issue order: MMA1_0, MMA2_0, then per tile t
-      //   MMA3_t, MMA4_t, MMA5_t, MMA1_{t+1}, MMA2_{t+1}
-      bool ok = mbar_wait_w(sm.kv_full(), 0, wc, ST_BWD_TIMEOUT_KV) && mbar_wait_w(sm.q_full(0), 0, wc, ST_BWD_TIMEOUT_Q);
-      if (ok) {
-        tc_fence_after();
-        mma_scores(tmem + L::TM_S, d_k, d_q);
-        umma_commit_w(sm.s_full());
-        ok = mbar_wait_w(sm.do_full(0), 0, wc, ST_BWD_TIMEOUT_Q);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
+        umma_ss_w(d_tm, a + off, b + off, IDESC_S, kk > 0 ? 1u : 0u);
       }
-      if (ok) {
-        tc_fence_after();
-        mma_scores(tmem + L::TM_DP, d_v, d_do);
-        umma_commit_w(sm.dp_full());
-      }
-      for (int t = 0; ok && t < n_it; ++t) {
-        const int st = t % STAGES, st1 = (t + 1) % STAGES;
-        const uint32_t ph = t & 1, ph1 = ((t + 1) / STAGES) & 1;
+    };
+    // Per item: MMA1_0, MMA2_0, then per tile t
+    //   MMA3_t, MMA4_t, MMA5_t, MMA1_{t+1}, MMA2_{t+1}
+    // T0 is the CTA-wide index of the item's first query tile.
+    int T0 = 0, ni = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < n_items; ++k) {
+      const int n_it = bwd_item<L::BN, L::BM>(p, sc, k).n_it;
+      if (n_it == 0) continue;
+      const int s0 = T0 % STAGES;
+      const uint32_t ph0 = (T0 / STAGES) & 1;
+      ok = mbar_wait_w(sm.kv_full(), ni & 1, wc, ST_BWD_TIMEOUT_KV) &&
+           mbar_wait_w(sm.q_full(s0), ph0, wc, ST_BWD_TIMEOUT_Q);
+      if (!ok) break;
+      tc_fence_after();
+      // S columns: the previous item's last P^T was read by its MMA3, issued before
+      mma_scores(tmem + L::TM_S, d_k, d_q + s0 * TILE16);
+      umma_commit_w(sm.s_full());
+      // dP columns: the previous item's last dQ^T must have been read out
+      ok = (T0 == 0 || mbar_wait_w(sm.dq_empty(), (T0 - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) &&
+           mbar_wait_w(sm.do_full(s0), ph0, wc, ST_BWD_TIMEOUT_Q);
+      if (!ok) break;
+      tc_fence_after();
+      mma_scores(tmem + L::TM_DP, d_v, d_do + s0 * TILE16);
+      umma_commit_w(sm.dp_full());
+      for (int t = 0; t < n_it; ++t) {
+        const int T = T0 + t;
+        const int st = T % STAGES, st1 = (T + 1) % STAGES;
+        const uint32_t ph = T & 1, ph1 = ((T + 1) / STAGES) & 1;
         const bool next = t + 1 < n_it;
-        // MMA3: dV += P^T_t dO_t.  A = P^T from tensor memory: queries 0-63 in
+        // MMA3: dV += P^T_t dO_t (dV starts over at t = 0: the warpgroups
+        // arrive on p_full for an item only after writing out the previous
+        // item's dV and dK).  A = P^T from tensor memory: queries 0-63 in
         // columns [0, 32), queries 64-127 in [64, 96) (each half in its own
         // S columns); B = dO_t MN-major (16 queries = 2 KB per step).
-        if (!mbar_wait_w(sm.p_full(), ph, wc, ST_BWD_TIMEOUT_P)) break;
+        if (!mbar_wait_w(sm.p_full(), ph, wc, ST_BWD_TIMEOUT_P)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < L::BM / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
           umma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + pcol, m_do + st * TILE16 + kk * (2048 >> 4), IDESC_G,
-                  (t > 0 || kk > 0) ? 1u : 0u);
+                    (t > 0 || kk > 0) ? 1u : 0u);
         }
-        if (!mbar_wait_w(sm.ds_full(), ph, wc, ST_BWD_TIMEOUT_DS)) break;
+        if (!mbar_wait_w(sm.ds_full(), ph, wc, ST_BWD_TIMEOUT_DS)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         // MMA4: dK += dS^T_t Q_t.  A = dS^T (bf16) from the dP columns, laid out
         // like P^T; B = Q_t MN-major.
@@ -443,7 +487,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < L::BM / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
           umma_ts_w(tmem + L::TM_DK, tmem + L::TM_DP + pcol, m_q + st * TILE16 + kk * (2048 >> 4), IDESC_G,
-                  (t > 0 || kk > 0) ? 1u : 0u);
+                    (t > 0 || kk > 0) ? 1u : 0u);
         }
         // MMA5: dQ^T_t = K^T dS_t into the dP columns, after MMA4 has read dS^T
         // there.  A = K MN-major, B = dS^T read as [query][key] MN-major (two
@@ -456,24 +500,34 @@ __global__ void __launch_bounds__(384, 1)
         if (next) {
           // MMA1: S^T_{t+1} into the S columns (P^T_t was read by MMA3_t, issued
           // before: the tensor cores run in issue order).
-          if (!mbar_wait_w(sm.q_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          if (!mbar_wait_w(sm.q_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           mma_scores(tmem + L::TM_S, d_k, d_q + st1 * TILE16);
           umma_commit_w(sm.s_full());
           // MMA2: dP^T_{t+1} into the dP columns once dQ^T_t has been read out.
           // Its commit also covers MMA5_t, the last reader of the dS buffer.
-          if (!mbar_wait_w(sm.dq_empty(), ph, wc, ST_BWD_TIMEOUT_DQE)) break;
-          if (!mbar_wait_w(sm.do_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) break;
+          if (!mbar_wait_w(sm.dq_empty(), ph, wc, ST_BWD_TIMEOUT_DQE) ||
+              !mbar_wait_w(sm.do_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           mma_scores(tmem + L::TM_DP, d_v, d_do + st1 * TILE16);
           umma_commit_w(sm.dp_full());
         }
       }
-      umma_commit_w(sm.dkv_done());
-      // nothing may be in flight on the tensor cores when the CTA frees TMEM
-      umma_commit_w(sm.drain());
-      if (!mbar_wait_drain(sm.drain(), 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
+      if (!ok) break;
+      umma_commit_w(sm.dkv_done());  // dV, dK of the item are complete
+      umma_commit_w(sm.kv_free());   // K and V are no longer read
+      T0 += n_it;
+      ++ni;
     }
+    // nothing may be in flight on the tensor cores when the CTA frees TMEM
+    umma_commit_w(sm.drain());
+    if (!mbar_wait_drain(sm.drain(), 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
     tc_fence_before();
     cta_bar_sync<384>();
     tc_fence_after();
@@ -482,30 +536,46 @@ __global__ void __launch_bounds__(384, 1)
     reg_lower<BWD_REGS_LOW>();
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
     const uint32_t sbase = sm.base;
-    const BwdTile g = bwd_tile<L::BN, L::BM>(p);
-    const int bh = g.bh, i0 = g.i0, n_it = g.n_it;
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
     // ----------------------------------------------------- dQ reduce-adds --
     // Per tile: the half staged in Q_t's buffer (queries 64-127) first, then the
     // half in dO_t's buffer (0-63); each buffer goes back to the producer once
     // its reduce-add has read it.  Q_{t+2} is needed sooner than dO_{t+2} (its
-    // S^T product comes first), so Q_t's buffer is released first.  A reduce-add
-    // reads its 32 KB at about 25 bytes per cycle (the SM's rate for reductions
-    // into global memory), so the two take about as long as the tile's products.
-    if (lane == 0 && n_it > 0) {
-      for (int t = 0; t < n_it; ++t) {
-        const int st = t % STAGES;
-        const int q0 = (i0 + t) * L::BM;
-        if (!mbar_wait(sm.red_ready(1), t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
-        tma_reduce_add_3d(&tm_dq, sbase + L::OFF_Q + st * L::TILE, 0, q0 + 64, bh);
-        bulk_commit_group();
-        if (!mbar_wait(sm.red_ready(0), t & 1, wc, ST_BWD_TIMEOUT_RED)) break;
-        tma_reduce_add_3d(&tm_dq, sbase + L::OFF_DO + st * L::TILE, 0, q0, bh);
-        bulk_commit_group();
-        bulk_wait_read<1>();
-        mbar_arrive(sm.q_empty(st));
-        bulk_wait_read<0>();
-        mbar_arrive(sm.do_empty(st));
+    // S^T product comes first), and the SM's TMA unit serves its requests in
+    // order, so within an item the load of Q_{t+2} is let in between the two
+    // reduce-adds: the second one is issued only after the producer has issued
+    // that load.  A reduce-add reads its 32 KB at about 20-25 bytes per cycle
+    // (the SM's rate for reductions into global memory), so the two take about
+    // as long as the tile's products.
+    if (lane == 0) {
+      int T0 = 0;
+      bool go = true;
+      for (int k = 0; go && k < n_items; ++k) {
+        const BwdItem g = bwd_item<L::BN, L::BM>(p, sc, k);
+        for (int t = 0; t < g.n_it; ++t) {
+          const int T = T0 + t;
+          const int st = T % STAGES;
+          const int q0 = (g.i0 + t) * L::BM;
+          if (!mbar_wait(sm.red_ready(1), T & 1, wc, ST_BWD_TIMEOUT_RED)) {
+            go = false;
+            break;
+          }
+          tma_reduce_add_3d(&tm_dq, sbase + L::OFF_Q + st * L::TILE, 0, q0 + 64, g.bh);
+          bulk_commit_group();
+          bulk_wait_read<0>();
+          mbar_arrive(sm.q_empty(st));
+          if ((t + STAGES < g.n_it && !mbar_wait(sm.q_issued(), (T + STAGES) & 1, wc, ST_BWD_TIMEOUT_RED)) ||
+              !mbar_wait(sm.red_ready(0), T & 1, wc, ST_BWD_TIMEOUT_RED)) {
+            go = false;
+            break;
+          }
+          tma_reduce_add_3d(&tm_dq, sbase + L::OFF_DO + st * L::TILE, 0, q0, g.bh);
+          bulk_commit_group();
+          bulk_wait_read<0>();
+          mbar_arrive(sm.do_empty(st));
+        }
+        T0 += g.n_it;
       }
       // the CTA may not exit while a reduce-add still reads its shared memory
       bulk_wait_all();
@@ -515,9 +585,8 @@ __global__ void __launch_bounds__(384, 1)
     reg_raise<BWD_REGS_HIGH>();
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
     const uint32_t sbase = sm.base;
-    const BwdTile g = bwd_tile<L::BN, L::BM>(p);
-    const int bh = g.bh, k0 = g.k0, kv_limit = g.kv_limit, i0 = g.i0, n_it = g.n_it;
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ---------------------------------------------------- elementwise WGs --
     // Both warpgroups take every tile: warpgroup h owns query columns
@@ -528,183 +597,195 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + L::TM_S + h * 64;   // this half's S^T, then its P^T
     const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T, then dQ^T
-    const bool key_ok = (k0 + r) < kv_limit;
-    const int jrow = k0 + r - p.qoff + 1;  // causal: first visible query row of key k0 + r
     const float sl = p.scale_log2, scale = p.scale;
     const uint32_t ds_row = sbase + L::OFF_DS + h * L::COLBLK + r * 128;
     const uint32_t stat = sbase + L::OFF_STAT + h * 256;  // + stage * 1024: nl; + 512: nd
     bool ok = true;
-    // Pass t drains dQ^T_t, then forms P^T and dS^T of tile u = t + 1:
-    //   dQ^T_t -> staged row-major for its reduce-add  |  P^T_u  |  dS^T_u
-    // (dS^T_u waits for dP^T_u, which MMA2_u writes only after the drain, so
-    // P^T_u fits in that wait either way; this order keeps P^T_u's registers
-    // out of the drain.)
-    for (int t = -1; t < n_it; ++t) {
-      float pr[64];  // P^T_u of this thread's key row, from the first part to the last
-      const int u = t + 1;
-      const int su = u % STAGES;
-      const int qu = (i0 + u) * L::BM + h * 64;  // first query of this half of tile u
-      if (t >= 0) {
-        // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows.
-        // Stage them row-major -- warpgroup 0 in dO_t's buffer, warpgroup 1 in
-        // Q_t's buffer, both free since every reader of Q_t and dO_t ran before
-        // MMA5_t -- for one tiled reduce-add into global dQ each (rows past N are
-        // skipped by the tensor map).  A warp's 32 lanes write 128 consecutive
-        // bytes per store; after the second load the dP columns are free for
-        // MMA2_{t+1}.
-        if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), t & 1, wc, ST_BWD_TIMEOUT_DQ))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t out_row = sbase + (h == 0 ? L::OFF_DO : L::OFF_Q) + (t % STAGES) * L::TILE + r * 4;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t qr[32];
-          FA_TMEM_LD32(dp_col + half * 32, qr);
-          tmem_wait_ld();
-          FA_REG_FENCE32(qr);
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(sm.dq_empty());
+    int T0 = 0, ni = 0;
+    for (int k = 0; ok && k < n_items; ++k) {
+      const BwdItem g = bwd_item<L::BN, L::BM>(p, sc, k);
+      const int bh = g.bh, k0 = g.k0, i0 = g.i0, n_it = g.n_it;
+      const bool key_ok = (k0 + r) < g.kv_limit;
+      const int jrow = k0 + r - p.qoff + 1;  // causal: first visible query row of key k0 + r
+      // Pass t drains dQ^T_t, then forms P^T and dS^T of tile u = t + 1:
+      //   dQ^T_t -> staged row-major for its reduce-add  |  P^T_u  |  dS^T_u
+      // (dS^T_u waits for dP^T_u, which MMA2_u writes only after the drain, so
+      // P^T_u fits in that wait either way; this order keeps P^T_u's registers
+      // out of the drain.)  T = T0 + t counts query tiles over the CTA's items.
+      for (int t = n_it > 0 ? -1 : 0; t < n_it; ++t) {
+        float pr[64];  // P^T_u of this thread's key row, from the second part to the last
+        const int u = t + 1;
+        const int T = T0 + t, U = T0 + u;
+        const int su = U % STAGES;
+        const int qu = (i0 + u) * L::BM + h * 64;  // first query of this half of tile u
+        if (t >= 0) {
+          // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows.
+          // Stage them row-major -- warpgroup 0 in dO_t's buffer, warpgroup 1 in
+          // Q_t's buffer, both free since every reader of Q_t and dO_t ran before
+          // MMA5_t -- for one tiled reduce-add into global dQ each (rows past N are
+          // skipped by the tensor map).  A warp's 32 lanes write 128 consecutive
+          // bytes per store; after the second load the dP columns are free for
+          // MMA2_{t+1}.
+          if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), T & 1, wc, ST_BWD_TIMEOUT_DQ))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const uint32_t out_row = sbase + (h == 0 ? L::OFF_DO : L::OFF_Q) + (T % STAGES) * L::TILE + r * 4;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) st_shared_f32(out_row + (half * 32 + j) * 512, __uint_as_float(qr[j]));
+          for (int half = 0; half < 2; ++half) {
+            uint32_t qr[32];
+            FA_TMEM_LD32(dp_col + half * 32, qr);
+            tmem_wait_ld();
+            FA_REG_FENCE32(qr);
+            if (half == 1) {
+              tc_fence_before();
+              mbar_arrive(sm.dq_empty());
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) st_shared_f32(out_row + (half * 32 + j) * 512, __uint_as_float(qr[j]));
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(sm.red_ready(h));
         }
-        fence_proxy_async_smem();
-        mbar_arrive(sm.red_ready(h));
-      }
 
-      if (u < n_it) {
-        // q_full is already complete here (S^T_u exists); waiting on it makes the
-        // stage's nl / nd rows visible to these threads
-        if (!__all_sync(0xffffffffu, mbar_wait(sm.s_full(), u & 1, wc, ST_BWD_TIMEOUT_S) &&
-                                         mbar_wait(sm.q_full(su), (u / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // causal: key k0 + r is visible to query qu + j iff k0 + r < qu + j + qoff
-        const int jmin = p.causal ? jrow - qu : -1;
-        // only tiles on the diagonal or past a key-padding edge mask anything
-        const bool masked = __any_sync(0xffffffffu, !key_ok || jmin > 0);
-        const uint32_t nl_s = stat + su * 1024;
-        const uint64_t sl2 = f2_pack(sl, sl);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sr[32];
-          FA_TMEM_LD32(s_col + half * 32, sr);
-          tmem_wait_ld();
-          FA_REG_FENCE32(sr);
-          if (masked) {
-#pragma unroll
-            for (int w = 0; w < 32; ++w)
-              if (!key_ok || half * 32 + w < jmin) sr[w] = __float_as_uint(-INFINITY);
+        if (u < n_it) {
+          // q_full is already complete here (S^T_u exists); waiting on it makes the
+          // stage's nl / nd rows visible to these threads
+          if (!__all_sync(0xffffffffu, mbar_wait(sm.s_full(), U & 1, wc, ST_BWD_TIMEOUT_S) &&
+                                           mbar_wait(sm.q_full(su), (U / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          // causal: key k0 + r is visible to query qu + j iff k0 + r < qu + j + qoff
+          const int jmin = p.causal ? jrow - qu : -1;
+          // only tiles on the diagonal or past a key-padding edge mask anything
+          const bool masked = __any_sync(0xffffffffu, !key_ok || jmin > 0);
+          const uint32_t nl_s = stat + su * 1024;
+          const uint64_t sl2 = f2_pack(sl, sl);
 #pragma unroll
-          for (int j4 = 0; j4 < 32; j4 += 4) {
-            float nl[4];
-            ld_shared_v4f(nl_s + (half * 32 + j4) * 4, nl);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t sr[32];
+            FA_TMEM_LD32(s_col + half * 32, sr);
+            tmem_wait_ld();
+            FA_REG_FENCE32(sr);
+            if (masked) {
 #pragma unroll
-            for (int w = 0; w < 4; w += 2) {
-              const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
-                                         f2_pack(nl[w], nl[w + 1]));
-              constexpr int E = FA_BWD_EXP2_FMA_EVERY > 0 ? FA_BWD_EXP2_FMA_EVERY : 1;
-              if (FA_BWD_EXP2_FMA_EVERY > 0 && ((j4 + w) / 2 + 1) % E == 0) {
-                f2_unpack(exp2_fma2(x2), pr[half * 32 + j4 + w], pr[half * 32 + j4 + w + 1]);  // FMA pipe
-              } else {
-                float x0, x1;
-                f2_unpack(x2, x0, x1);
-                pr[half * 32 + j4 + w] = ex2_approx(x0);
-                pr[half * 32 + j4 + w + 1] = ex2_approx(x1);
+              for (int w = 0; w < 32; ++w)
+                if (!key_ok || half * 32 + w < jmin) sr[w] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int j4 = 0; j4 < 32; j4 += 4) {
+              float nl[4];
+              ld_shared_v4f(nl_s + (half * 32 + j4) * 4, nl);
+#pragma unroll
+              for (int w = 0; w < 4; w += 2) {
+                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
+                                           f2_pack(nl[w], nl[w + 1]));
+                constexpr int E = FA_BWD_EXP2_FMA_EVERY > 0 ? FA_BWD_EXP2_FMA_EVERY : 1;
+                if (FA_BWD_EXP2_FMA_EVERY > 0 && ((j4 + w) / 2 + 1) % E == 0) {
+                  f2_unpack(exp2_fma2(x2), pr[half * 32 + j4 + w], pr[half * 32 + j4 + w + 1]);  // FMA pipe
+                } else {
+                  float x0, x1;
+                  f2_unpack(x2, x0, x1);
+                  pr[half * 32 + j4 + w] = ex2_approx(x0);
+                  pr[half * 32 + j4 + w + 1] = ex2_approx(x1);
+                }
               }
             }
           }
-        }
-        uint32_t pk[32];
+          uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
-        FA_TMEM_ST32(s_col, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(sm.p_full());
-      }
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+          FA_TMEM_ST32(s_col, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(sm.p_full());
 
-      if (u < n_it) {
-        // dP^T_u; its commit also covers MMA5_t, so the dS buffer is free
-        if (!__all_sync(0xffffffffu, mbar_wait(sm.dp_full(), u & 1, wc, ST_BWD_TIMEOUT_DP))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t nd_s = stat + su * 1024 + 512;
-        const uint64_t sc2 = f2_pack(scale, scale);
-        uint32_t dsk[32];
+          // dP^T_u; its commit also covers MMA5_t, so the dS buffer is free
+          if (!__all_sync(0xffffffffu, mbar_wait(sm.dp_full(), U & 1, wc, ST_BWD_TIMEOUT_DP))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t nd_s = stat + su * 1024 + 512;
+          const uint64_t sc2 = f2_pack(scale, scale);
+          uint32_t dsk[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t dpr[32];
-          FA_TMEM_LD32(dp_col + half * 32, dpr);
-          tmem_wait_ld();
-          FA_REG_FENCE32(dpr);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t dpr[32];
+            FA_TMEM_LD32(dp_col + half * 32, dpr);
+            tmem_wait_ld();
+            FA_REG_FENCE32(dpr);
 #pragma unroll
-          for (int j4 = 0; j4 < 32; j4 += 4) {
-            const int j = half * 32 + j4;
-            float nd[4];
-            ld_shared_v4f(nd_s + j * 4, nd);
+            for (int j4 = 0; j4 < 32; j4 += 4) {
+              const int j = half * 32 + j4;
+              float nd[4];
+              ld_shared_v4f(nd_s + j * 4, nd);
 #pragma unroll
-            for (int w = 0; w < 4; w += 2) {
-              // dS = P (dP scale - D scale)
-              const uint64_t g =
-                  f2_mul(f2_fma(f2_pack(__uint_as_float(dpr[j4 + w]), __uint_as_float(dpr[j4 + w + 1])), sc2,
-                                f2_pack(nd[w], nd[w + 1])),
-                         f2_pack(pr[j + w], pr[j + w + 1]));
-              float g0, g1;
-              f2_unpack(g, g0, g1);
-              dsk[(j + w) / 2] = pack_bf16x2(g0, g1);
+              for (int w = 0; w < 4; w += 2) {
+                // dS = P (dP scale - D scale)
+                const uint64_t g =
+                    f2_mul(f2_fma(f2_pack(__uint_as_float(dpr[j4 + w]), __uint_as_float(dpr[j4 + w + 1])), sc2,
+                                  f2_pack(nd[w], nd[w + 1])),
+                           f2_pack(pr[j + w], pr[j + w + 1]));
+                float g0, g1;
+                f2_unpack(g, g0, g1);
+                dsk[(j + w) / 2] = pack_bf16x2(g0, g1);
+              }
             }
           }
-        }
-        // dS^T as MMA4's A operand: bf16 pairs into the first 32 of this half's
-        // dP columns (dP^T has been read into registers) ...
-        FA_TMEM_ST32(dp_col, dsk);
-        // ... and as MMA5's B operand: row r of this half's 128B-swizzled block,
-        // 16-byte chunk c at c ^ (r & 7).
+          // dS^T as MMA4's A operand: bf16 pairs into the first 32 of this half's
+          // dP columns (dP^T has been read into registers) ...
+          FA_TMEM_ST32(dp_col, dsk);
+          // ... and as MMA5's B operand: row r of this half's 128B-swizzled block,
+          // 16-byte chunk c at c ^ (r & 7).
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
-        tmem_wait_st();
-        tc_fence_before();
-        fence_proxy_async_smem();
-        mbar_arrive(sm.ds_full());
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
+          tmem_wait_st();
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive(sm.ds_full());
+        }
       }
-    }
 
-    // ------------------------------------------------------------ epilogue --
-    // warpgroup 0 writes dV, warpgroup 1 writes dK: TMEM lane r = key row k0 + r
-    if (ok && n_it > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.dkv_done(), 0, wc, ST_BWD_TIMEOUT_DONE))) ok = false;
-    if (ok) {
-      tc_fence_after();
-      const int key = k0 + r;
-      float* out = (h == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D;
-      const uint32_t col = lane_base + (h == 0 ? L::TM_DV : L::TM_DK);
+      // ---------------------------------------------------------- epilogue --
+      // warpgroup 0 writes dV, warpgroup 1 writes dK: TMEM lane r = key row k0 + r
+      if (ok && n_it > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.dkv_done(), ni & 1, wc, ST_BWD_TIMEOUT_DONE)))
+        ok = false;
+      if (ok) {
+        tc_fence_after();
+        const int key = k0 + r;
+        float* out = (h == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D;
+        const uint32_t col = lane_base + (h == 0 ? L::TM_DV : L::TM_DK);
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t v[32];
-        if (n_it > 0) {
-          FA_TMEM_LD32(col + cb * 32, v);
-          tmem_wait_ld();
-          FA_REG_FENCE32(v);
-        } else {
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t v[32];
+          if (n_it > 0) {
+            FA_TMEM_LD32(col + cb * 32, v);
+            tmem_wait_ld();
+            FA_REG_FENCE32(v);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (key < p.Nk) {
+            float4* o4 = reinterpret_cast<float4*>(out + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
         }
-        if (key < p.Nk) {
-          float4* o4 = reinterpret_cast<float4*>(out + cb * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-        }
+        // the next item's first MMA3 / MMA4 overwrite dV and dK only after these
+        // warpgroups' p_full for it, i.e. after these loads
+        tc_fence_before();
+      }
+      if (n_it > 0) {
+        T0 += n_it;
+        ++ni;
       }
     }
     tc_fence_before();

@@ -255,44 +255,34 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
   return FA_OK;
 }
 
-// Work list of a persistent forward launch (see fa::FwdSched), built on the
-// host once per problem shape.  Items are weighted by the key tiles their two
-// query tiles process, plus two for the item's fixed costs; the kv_len values
-// live on the device and are not looked at (a padded problem just balances
-// less well).  Heads are taken in groups whose K and V fit in about 48 MB, so
-// that the CTAs working at one time share them in L2; within a group the items
-// go heaviest first, each to the CTA with the least work so far.
-struct SchedKey {
-  int BH, N, Nk, causal, qoff, D, G;
-  bool operator<(const SchedKey& o) const {
-    return std::tie(BH, N, Nk, causal, qoff, D, G) < std::tie(o.BH, o.N, o.Nk, o.causal, o.qoff, o.D, o.G);
+// Work list of a persistent launch (fa::WorkList), built on the host once per
+// problem shape and kind of kernel.  weights[u] is the work of unit u of a head
+// (key tiles processed, plus two for an item's fixed costs); kv_len values live
+// on the device and are not looked at (a padded problem just balances less
+// well).  Heads are taken in groups whose operands (head_bytes each) fit in
+// about 48 MB of L2; within a group the items go heaviest first, each to the
+// CTA with the least work so far.
+struct WorkKey {
+  int kind, BH, N, Nk, causal, qoff, D, G;
+  bool operator<(const WorkKey& o) const {
+    return std::tie(kind, BH, N, Nk, causal, qoff, D, G) <
+           std::tie(o.kind, o.BH, o.N, o.Nk, o.causal, o.qoff, o.D, o.G);
   }
 };
-std::map<SchedKey, std::unique_ptr<fa::FwdSched>> g_sched;
-std::mutex g_sched_mu;
+std::map<WorkKey, std::unique_ptr<fa::WorkList>> g_work;
+std::mutex g_work_mu;
 
-const fa::FwdSched* fwd_schedule(int BH, int N, int Nk, int causal, int qoff, int D, int G) {
-  const SchedKey key{BH, N, Nk, causal, qoff, D, G};
-  std::lock_guard<std::mutex> lk(g_sched_mu);
-  auto found = g_sched.find(key);
-  if (found != g_sched.end()) return found->second.get();
-  auto sc = std::make_unique<fa::FwdSched>();
-  const int n_qt = (N + 127) / 128, n_pair = (n_qt + 1) / 2;
-  const long long n_items = static_cast<long long>(BH) * n_pair;
-  sc->n_items = static_cast<int>(n_items);
-  sc->table = 0;
-  if (n_items <= fa::FWD_SCHED_MAX_ITEMS && G <= fa::FWD_SCHED_MAX_CTAS) {
-    const int n_kv_all = (Nk + 127) / 128;
-    auto tiles = [&](int qt) -> int {  // as the kernel computes it, without kv_len
-      if (qt >= n_qt) return 0;
-      if (!causal) return n_kv_all;
-      const int last_key = std::min(qt * 128 + 128, N) - 1 + qoff - 1;
-      return last_key < 0 ? 0 : std::min(n_kv_all, last_key / 128 + 1);
-    };
-    std::vector<int> w(n_pair);
-    for (int pr = 0; pr < n_pair; ++pr) w[pr] = tiles(2 * pr) + tiles(2 * pr + 1) + 2;
-    const double kv_head = 2.0 * Nk * D * 2;
-    const int hpg = std::max(1, static_cast<int>(48.0 * 1024 * 1024 / kv_head));
+const fa::WorkList* work_list(const WorkKey& key, const std::vector<int>& weights, double head_bytes) {
+  std::lock_guard<std::mutex> lk(g_work_mu);
+  auto found = g_work.find(key);
+  if (found != g_work.end()) return found->second.get();
+  auto wl = std::make_unique<fa::WorkList>();
+  const int BH = key.BH, G = key.G, units = static_cast<int>(weights.size());
+  const long long n_items = static_cast<long long>(BH) * units;
+  wl->n_items = static_cast<int>(n_items);
+  wl->table = 0;
+  if (n_items <= fa::WL_MAX_ITEMS && G <= fa::WL_MAX_CTAS) {
+    const int hpg = std::max(1, static_cast<int>(48.0 * 1024 * 1024 / head_bytes));
     std::vector<std::vector<uint32_t>> lists(G);
     using Load = std::pair<long long, int>;  // (work so far, CTA)
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
@@ -301,7 +291,7 @@ const fa::FwdSched* fwd_schedule(int BH, int N, int Nk, int causal, int qoff, in
     for (int g0 = 0; g0 < BH; g0 += hpg) {
       group.clear();
       for (int bh = g0; bh < std::min(BH, g0 + hpg); ++bh)
-        for (int pr = n_pair - 1; pr >= 0; --pr) group.push_back({w[pr], static_cast<uint32_t>(bh * n_pair + pr)});
+        for (int u = 0; u < units; ++u) group.push_back({weights[u], static_cast<uint32_t>(bh * units + u)});
       std::stable_sort(group.begin(), group.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
       for (const auto& it : group) {
         Load ld = heap.top();
@@ -312,15 +302,44 @@ const fa::FwdSched* fwd_schedule(int BH, int N, int Nk, int causal, int qoff, in
     }
     int pos = 0;
     for (int c = 0; c < G; ++c) {
-      sc->start[c] = static_cast<uint16_t>(pos);
-      for (uint32_t id : lists[c]) sc->list[pos++] = id;
+      wl->start[c] = static_cast<uint16_t>(pos);
+      for (uint32_t id : lists[c]) wl->list[pos++] = id;
     }
-    sc->start[G] = static_cast<uint16_t>(pos);
-    sc->table = 1;
+    wl->start[G] = static_cast<uint16_t>(pos);
+    wl->table = 1;
   }
-  const fa::FwdSched* out = sc.get();
-  g_sched[key] = std::move(sc);
+  const fa::WorkList* out = wl.get();
+  g_work[key] = std::move(wl);
   return out;
+}
+
+// Key tiles query tile qt needs, as the kernels compute it (without kv_len).
+int tiles_needed(int qt, int n_qt, int N, int Nk, int causal, int qoff) {
+  const int n_kv_all = (Nk + 127) / 128;
+  if (qt >= n_qt) return 0;
+  if (!causal) return n_kv_all;
+  const int last_key = std::min(qt * 128 + 128, N) - 1 + qoff - 1;
+  return last_key < 0 ? 0 : std::min(n_kv_all, last_key / 128 + 1);
+}
+
+const fa::WorkList* fwd_work_list(int BH, int N, int Nk, int causal, int qoff, int D, int G) {
+  const int n_qt = (N + 127) / 128, n_pair = (n_qt + 1) / 2;
+  std::vector<int> w(n_pair);
+  for (int pr = 0; pr < n_pair; ++pr)
+    w[pr] = tiles_needed(2 * pr, n_qt, N, Nk, causal, qoff) + tiles_needed(2 * pr + 1, n_qt, N, Nk, causal, qoff) + 2;
+  return work_list(WorkKey{0, BH, N, Nk, causal, qoff, D, G}, w, 2.0 * Nk * D * 2);  // K and V of a head
+}
+
+const fa::WorkList* bwd_work_list(int BH, int N, int Nk, int causal, int qoff, int D, int G) {
+  const int n_qt = (N + 127) / 128, n_kt = (Nk + 127) / 128;
+  std::vector<int> w(n_kt);
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int k0 = kt * 128;
+    const int i0 = causal ? std::max(0, k0 - qoff + 1) / 128 : 0;
+    w[kt] = ((k0 < Nk && i0 < n_qt) ? n_qt - i0 : 0) + 2;
+  }
+  // Q, dO, K and V of a head
+  return work_list(WorkKey{1, BH, N, Nk, causal, qoff, D, G}, w, 2.0 * (N + Nk) * D * 2);
 }
 
 template <int D, int STAGES>
@@ -353,7 +372,7 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
   const long long n_items = static_cast<long long>((p.n_qt + 1) / 2) * BH;
   if (n_items > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "problem too large");
   const int G = static_cast<int>(std::min<long long>(std::max(1, ds.sm_count), n_items));
-  const fa::FwdSched* sc = fwd_schedule(BH, N, Nk, causal, p.qoff, D, G);
+  const fa::WorkList* sc = fwd_work_list(BH, N, Nk, causal, p.qoff, D, G);
   fa::fwd_bf16_tc_kernel<D, STAGES><<<static_cast<unsigned>(G), 384, L::BYTES, stream>>>(mq, mk, mv, p, *sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch fwd_bf16_tc_kernel");
@@ -386,8 +405,10 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   const long long Np = bwd_np(N);
   const long long pre_blocks = static_cast<long long>(BH) * (Np / 64);
   const long long n_kt = (Nk + L::BN - 1) / L::BN;
-  const long long blocks = n_kt * BH;
-  if (pre_blocks > 0x7fffffffll || blocks > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  const long long n_items = n_kt * BH;
+  if (pre_blocks > 0x7fffffffll || n_items > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  // persistent grid: one CTA per SM, fewer when there are fewer key tiles
+  const int G = static_cast<int>(std::min<long long>(std::max(1, ds.sm_count), n_items));
 
   // every tensor map is built before anything is enqueued, so that a failure
   // here leaves the stream untouched
@@ -434,7 +455,9 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.load();
-  fa::bwd_bf16_tc_kernel<kStagesBwd><<<static_cast<unsigned>(blocks), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
+  const fa::WorkList* wl = bwd_work_list(BH, N, Nk, causal, p.qoff, D, G);
+  fa::bwd_bf16_tc_kernel<kStagesBwd>
+      <<<static_cast<unsigned>(G), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p, *wl);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_bf16_tc_kernel");
   return FA_OK;
 }

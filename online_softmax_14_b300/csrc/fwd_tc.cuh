@@ -16,9 +16,9 @@
 //
 // Scheduling (the Question bank's causal block-skipping item: under a causal
 // mask the query tiles of a head have unequal work).  The host gives every CTA
-// its item list (FwdSched): longest first within groups of heads whose K and V
-// fit in L2 together, each item to the CTA with the least work so far.  Items
-// run back to back: the producer loads the next item's Q as soon as the MMA warp
+// its item list (WorkList in worklist.cuh): longest first within groups of heads
+// whose K and V fit in L2 together, each item to the CTA with the least work so
+// far.  Items run back to back: the producer loads the next item's Q as soon as the MMA warp
 // has issued the last products reading the current one, the K/V ring runs on,
 // and the next item's first S products run while the softmax warpgroups write
 // the current item's O.
@@ -48,6 +48,7 @@
 #pragma once
 #include "exp2_poly.cuh"
 #include "ptx.cuh"
+#include "worklist.cuh"
 
 // Every FA_FWD_EXP2_FMA_EVERY-th pair of scores takes its exponentials on the FMA
 // pipe (exp2_fma2) instead of the special-function unit; 0 = none.
@@ -96,22 +97,6 @@ struct TcParams {
   int inject;         // test hook: 1 = producer stops after the first K/V tile
 };
 
-
-// The work of one launch: items are (batch*head, query-tile pair) and each CTA
-// of the persistent grid runs a list of them.  With `table`, CTA c runs
-// list[start[c] .. start[c+1]) in that order (the host builds it: longest first
-// within groups of heads whose K and V fit in L2 together, each item to the CTA
-// with the least work so far); without, CTA c runs items c, c + G, c + 2G, ...
-// of the head-major order, heaviest pair first within a head.  An item id is
-// bh * n_pair + pair.
-constexpr int FWD_SCHED_MAX_CTAS = 160;
-constexpr int FWD_SCHED_MAX_ITEMS = 6144;
-struct FwdSched {
-  int n_items;
-  int table;
-  uint16_t start[FWD_SCHED_MAX_CTAS + 1];
-  uint32_t list[FWD_SCHED_MAX_ITEMS];
-};
 
 // NS = number of K/V slots: K_j and V_j stream through one ring of tile-sized
 // slots in the order K_0, V_0, K_1, V_1, ... (continuing from one item to the
@@ -164,26 +149,10 @@ struct FwdItem {
   int n_max;
 };
 
-__device__ __forceinline__ int fwd_items_of_cta(const FwdSched& sc) {
-  const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
-  if (sc.table) return sc.start[c + 1] - sc.start[c];
-  return c < sc.n_items ? (sc.n_items - 1 - c) / G + 1 : 0;
-}
-
 template <int BM, int BN>
-__device__ __forceinline__ FwdItem fwd_item(const TcParams& p, const FwdSched& sc, int k) {
-  const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
-  const int n_pair = (p.n_qt + 1) >> 1;
-  int bh, pr;
-  if (sc.table) {
-    const int id = static_cast<int>(sc.list[sc.start[c] + k]);
-    bh = id / n_pair;
-    pr = id % n_pair;
-  } else {
-    const int i = c + k * G;  // head-major, heaviest pair first within a head
-    bh = i / n_pair;
-    pr = n_pair - 1 - i % n_pair;
-  }
+__device__ __forceinline__ FwdItem fwd_item(const TcParams& p, const WorkList& sc, int k) {
+  int bh, pr;  // units of a head: its query-tile pairs, the last one heaviest under a causal mask
+  wl_item(sc, k, (p.n_qt + 1) >> 1, true, bh, pr);
   FwdItem it;
   it.bh = bh;
   it.q0 = pr * 2 * BM;
@@ -208,7 +177,7 @@ template <int D, int NS>
 __global__ void __launch_bounds__(384, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const TcParams p,
-                        const __grid_constant__ FwdSched sc) {
+                        const __grid_constant__ WorkList sc) {
   using L = TcLayout<D, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -258,7 +227,7 @@ __global__ void __launch_bounds__(384, 1)
     reg_lower<FWD_REGS_LOW>();
     const FwdSmem<D, NS> sm(smem_u32_fresh(smem_raw));
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
-    const int n_items = fwd_items_of_cta(sc);
+    const int n_items = wl_count(sc);
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       int c = 0, nq = 0;  // K/V loads, Q loads issued
@@ -311,7 +280,7 @@ __global__ void __launch_bounds__(384, 1)
     reg_lower<FWD_REGS_LOW>();
     const FwdSmem<D, NS> sm(smem_u32_fresh(smem_raw));
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
-    const int n_items = fwd_items_of_cta(sc);
+    const int n_items = wl_count(sc);
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ---------------------------------------------------------- MMA issuer --
     // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
@@ -432,7 +401,7 @@ __global__ void __launch_bounds__(384, 1)
     reg_raise<FWD_REGS_HIGH>();
     const FwdSmem<D, NS> sm(smem_u32_fresh(smem_raw));
     const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
-    const int n_items = fwd_items_of_cta(sc);
+    const int n_items = wl_count(sc);
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ------------------------------------------------------------- softmax --
     const int ti = warp >> 2;          // query tile 0 or 1 (warps 10-11 have no role)
