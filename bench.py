@@ -54,15 +54,33 @@ BWD_WORKLOAD = "bf16_causal_fwdbwd_B4_H16_N4096_d128"
 FALLBACK_BF16_TFLOPS = 1800.0  # used only when MEASURED_PEAKS.json is absent
 L2_BYTES = 126 * 1024 * 1024
 
-# DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture,
-# valid only for the forward kernel sources whose digest is recorded with it.
-# The N=8192 launch was not captured itself: B=2 H=32 N=4096 (same kernel, half
-# the units) read 201,429,248 and wrote 49,031,680 bytes, and the traffic scales
-# with B*H*N*d (Q, K, V read once, O written once; K/V re-reads hit L2).
-NCU_TRAFFIC = {"bf16_causal_B2_H32_N8192_d128": {"bytes": 2 * (201429248 + 49031680),
-                                                 "src_digest": "ad9074c152faa792",
-                                                 "how": "scaled x2 from an ncu capture of B=2 H=32 N=4096"}}
-FWD_SOURCES = ("fwd_tc.cuh", "ptx.cuh", "fa_lib.cu")
+# DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture
+# of that launch, valid only for the forward sources whose digest is recorded
+# with it (kernel_src_digest).
+NCU_TRAFFIC = {"bf16_causal_B2_H32_N8192_d128": {"bytes": 450793472 + 115639552,
+                                                 "src_digest": "dfcd45f9750fe427",
+                                                 "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                                                        "one launch of this workload"}}
+# What the forward kernel is built from: its headers, and the host functions of
+# fa_lib.cu that shape its launch (grid and work list).
+FWD_HEADERS = ("fwd_tc.cuh", "ptx.cuh", "worklist.cuh", "exp2_poly.cuh")
+FWD_HOST_FUNCTIONS = ("fa_status launch_tc(", "const fa::WorkList* work_list(", "int tiles_needed(",
+                      "const fa::WorkList* fwd_work_list(")
+
+
+def _function_text(src: str, head: str) -> str:
+    """The text of the C++ function whose definition starts with `head`, up to
+    its matching closing brace ('' when absent)."""
+    i = src.find(head)
+    if i < 0:
+        return ""
+    j = src.index("{", i)
+    depth = 0
+    for k in range(j, len(src)):
+        depth += {"{": 1, "}": -1}.get(src[k], 0)
+        if depth == 0:
+            return src[i:k + 1]
+    return src[i:]
 
 
 def flops_per_step(w) -> float:
@@ -92,11 +110,16 @@ def bwd_flops(w) -> float:
 
 
 def kernel_src_digest() -> str:
-    """Digest of the sources the forward kernel is built from."""
+    """Digest of the sources the forward kernel and its launch are built from."""
+    csrc = os.path.join(ROOT, "online_softmax_14_b300", "csrc")
     h = hashlib.sha256()
-    for name in FWD_SOURCES:
-        with open(os.path.join(ROOT, "online_softmax_14_b300", "csrc", name), "rb") as f:
+    for name in FWD_HEADERS:
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(csrc, "fa_lib.cu"), encoding="utf-8") as f:
+        lib = f.read()
+    for head in FWD_HOST_FUNCTIONS:
+        h.update(_function_text(lib, head).encode())
     return h.hexdigest()[:16]
 
 
@@ -392,7 +415,7 @@ def run_fwd_bwd(args, fa, dev, stream, dist):
     """Forward and backward of the training workload (bf16, causal, B=4 H=16
     N=4096 d=128, dO drawn after Q, K, V), each timed over --bwd-steps launches
     with CUDA events on the launching stream.  The backward is one fa_bwd call
-    (two kernels: the row preprocess and the main tensor-core kernel)."""
+    (three kernels: the row preprocess, dK/dV per key tile, dQ per query tile)."""
     w = WORKLOADS[BWD_WORKLOAD]
     if args.bwd_shape:
         B, H, N = (int(x) for x in args.bwd_shape.split(","))
@@ -434,7 +457,7 @@ def run_fwd_bwd(args, fa, dev, stream, dist):
             "fwd_tflops": round(ff / ms_f / 1e9, 2), "bwd_tflops": round(fb / ms_b / 1e9, 2),
             "fwd_bwd_tflops": round((ff + fb) / (ms_f + ms_b) / 1e9, 2),
             "flops": {"fwd": ff, "bwd": fb, "bwd_formula": "10*B*H*N^2*d, halved for causal"},
-            "gpu_launches_per_bwd": 2}
+            "gpu_launches_per_bwd": 3}
 
 
 FP32_FFMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # 148 SMs x 128 FP32 lanes x 2 FLOP (FMA) x 2.032 GHz

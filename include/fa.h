@@ -119,8 +119,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   q, k, v, o, dO : const bf16*, [B, H, N, d], 16-byte aligned; o and lse are
  *                    the outputs of fa_fwd for the same q, k, v, scale, causal.
  *   lse            : const float*, [B, H, N] (required).
- *   dq, dk, dv     : float*, [B, H, N, d], 16-byte aligned; written (dq is
- *                    zeroed by the call, then accumulated).
+ *   dq, dk, dv     : float*, [B, H, N, d], 16-byte aligned; every element is
+ *                    written once (contents on entry do not matter).  Each row
+ *                    is summed in a fixed order, so repeated calls agree bit
+ *                    for bit.  Three kernels: a row preprocess, one kernel per
+ *                    128-key tile for dK and dV, one per 128-query tile for dQ.
  *   workspace      : device memory of at least fa_bwd_workspace_size(B, H, N, d)
  *                    bytes, 16-byte aligned, owned by the caller; its contents
  *                    on entry do not matter and are overwritten.
@@ -253,8 +256,9 @@ void fa_set_wait_timeout_ms(int ms);
 /*
  * fa_debug_inject -- test hook.  code 1 makes the next fa_fwd bf16 launches'
  * producers stop feeding K/V tiles after the first one; code 2 makes the next
- * fa_bwd launches' producers stop feeding Q/dO tiles after the first one.
- * Either way the consumers' bounded waits run out, each CTA drains the copies
+ * fa_bwd launches' dK/dV producers stop feeding Q/dO tiles after the first one;
+ * code 3 makes their dQ producers stop feeding K/V tiles after the first one.
+ * Every way the consumers' bounded waits run out, each CTA drains the copies
  * and tensor-core work it has in flight, frees its tensor memory and exits, and
  * fa_check_device_error reports FA_ERR_TIMEOUT.  code 0 (the default) turns it
  * off.  Nothing faults, traps or hangs either way.

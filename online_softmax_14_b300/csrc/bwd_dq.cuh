@@ -1,0 +1,539 @@
+// BFloat16 attention backward, dQ part, on the 5th-generation tensor cores
+// (tcgen05, sm_103a).
+//
+// dQ_i = sum_j dS_ij K_j sums over keys, so it is formed per 128-query tile,
+// the way the forward forms O: the scores and probabilities of the tile are
+// recomputed key tile by key tile ("Question bank -- Flash attention and
+// efficient attention", the recomputation items), and dQ stays in tensor memory
+// until the last key tile has been added.  With nl_i = -lse_i log2(e) and
+// nd_i = -D_i scale from the backward preprocess:
+//     S_j  = Q K_j^T,   P_j = 2^(S_j scale log2e + nl),   dP_j = dO V_j^T,
+//     dS_j = P_j (dP_j scale + nd)  (= scale P_j (dP_j - D)),   dQ += dS_j K_j.
+// dQ is written once per row; the kernel needs no zeroed output and its result
+// does not depend on the order in which CTAs run.
+//
+// bwd_dq_kernel is persistent; a work item is (batch*head, 128-query tile).  Q of
+// the item sits in tensor memory (the elementwise warps write it there), dO in
+// shared memory; the key tiles K_j and V_j stream through TMA rings of three
+// slots each.  Per key tile the tensor cores run three MMAs (128 x 128 x 128):
+//     S_j  = Q K_j^T     (A = Q from tensor memory, B = K_j K-major)
+//     dP_j = dO V_j^T    (A = dO, B = V_j, both K-major in shared memory)
+//     dQ  += dS_j K_j    (A = dS_j, bf16 in tensor memory; B = K_j MN-major)
+// Shared-memory bandwidth, not the tensor cores, bounds this loop on B300: the
+// products read their shared-memory operands at up to 128 bytes per cycle per
+// SM, which the TMA writes of the next tiles share.  With Q in tensor memory a
+// key tile costs 128 KB of operand reads and 64 KB of TMA writes, about 1500
+// cycles, under the 1536 cycles of its three products; with Q in shared memory
+// it would cost 224 KB, about 1750.
+//
+// S, dP and dS each have their own tensor-memory columns, and the elementwise
+// warps hand each one back as soon as they have read it, so that S_{j+1} and
+// dP_{j+1} are formed while the warps still work on tile j.  The MMA warp issues,
+// per key tile j: S_{j+1} (once the warps have read S_j), dP_{j+1} (once they
+// have read dP_j), dQ_j (once dS_j is stored).
+//
+// Roles (384 threads):
+//   warp 0     TMA producer: dO per item; K_j and V_j in the order the products
+//              need them (K_0, V_0, K_1, V_1, ...).
+//   warp 1     MMA issuer (lane 0 of the converged warp) and tensor-memory owner.
+//   warps 2-3  no role.
+//   warps 4-7  elementwise warpgroup 0: keys 0-63 of every key tile, head-dim
+//              columns 0-63 of Q and dQ;
+//   warps 8-11 elementwise warpgroup 1: keys 64-127, head-dim columns 64-127.
+//              Thread r owns query row r (TMEM lane r):
+//                Q row (its half) -> tensor memory, once per item (for the
+//                next item while finishing the current one);
+//                P = 2^(S scale log2e + nl_r) with the causal / padding mask,
+//                kept in registers; dS = P (dP scale + nd_r) -> bf16 into the
+//                dS columns, where the dQ product reads it;
+//                at the end of an item, its row's half of dQ -> global memory.
+//
+// Tensor memory (512 columns, f32 unless noted):
+//   [0,64) Q (bf16 pairs)   [64,128) dS (bf16 pairs; keys 0-63 in [64,96),
+//   64-127 in [96,128))   [128,256) S_j   [256,384) dP_j   [384,512) dQ
+//
+// Every wait is bounded: a wait that runs out records a status bit, the CTA
+// drains what it has in flight and exits.
+#pragma once
+#include "bwd_tc.cuh"
+
+namespace fa {
+
+struct DqLayout {
+  static constexpr int D = 128;  // the group issue (ptx.cuh) covers K = 128 in 16 KB column blocks
+  static constexpr int BM = 128;                   // queries per item
+  static constexpr int BN = 128;                   // keys per tile
+  static constexpr int KB = D / 64;                // 128-byte column blocks
+  static constexpr int COLBLK = 128 * 128;         // 16 KB: 128 rows x 128 bytes
+  static constexpr int TILE = 128 * D * 2;         // 32 KB: a dO, K or V tile
+  static constexpr int NK = 3, NV = 3;             // K and V ring slots
+  static constexpr int OFF_DO = 0;
+  static constexpr int OFF_K = TILE;
+  static constexpr int OFF_V = OFF_K + NK * TILE;
+  static constexpr int OFF_BAR = OFF_V + NV * TILE;
+  // barriers: do_full, do_free, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready,
+  //           s_full, s_free, dp_full, dp_free, ds_full, ds_free, dq_done, drain
+  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 32 + 1024;  // room to align the base up to 1024 bytes
+  static constexpr uint32_t TM_Q = 0, TM_DS = 64, TM_S = 128, TM_DP = 256, TM_DQ = 384, TM_COLS = 512;
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+// Shared-memory addresses (32-bit) of the dQ kernel's buffers and barriers,
+// from the 1024-aligned base of its dynamic shared memory.
+struct DqSmem {
+  using L = DqLayout;
+  uint32_t base;
+  __device__ __forceinline__ explicit DqSmem(uint32_t raw) : base((raw + 1023u) & ~1023u) {}
+  __device__ __forceinline__ uint32_t bar(int i) const { return base + L::OFF_BAR + 8 * i; }
+  __device__ __forceinline__ uint32_t do_full() const { return bar(0); }
+  // every product of an item that reads dO has run (one phase per item)
+  __device__ __forceinline__ uint32_t do_free() const { return bar(1); }
+  __device__ __forceinline__ uint32_t k_full(int s) const { return bar(2 + s); }
+  __device__ __forceinline__ uint32_t k_empty(int s) const { return bar(2 + L::NK + s); }
+  __device__ __forceinline__ uint32_t v_full(int s) const { return bar(2 + 2 * L::NK + s); }
+  __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(2 + 2 * L::NK + L::NV + s); }
+  static constexpr int X = 2 + 2 * L::NK + 2 * L::NV;
+  // the item's Q is in tensor memory (one phase per item)
+  __device__ __forceinline__ uint32_t q_ready() const { return bar(X); }
+  __device__ __forceinline__ uint32_t s_full() const { return bar(X + 1); }
+  // the elementwise warps have read S_j / dP_j (one phase per key tile)
+  __device__ __forceinline__ uint32_t s_free() const { return bar(X + 2); }
+  __device__ __forceinline__ uint32_t dp_full() const { return bar(X + 3); }
+  __device__ __forceinline__ uint32_t dp_free() const { return bar(X + 4); }
+  __device__ __forceinline__ uint32_t ds_full() const { return bar(X + 5); }
+  // the dQ product of key tile j has run: the dS columns are free
+  __device__ __forceinline__ uint32_t ds_free() const { return bar(X + 6); }
+  __device__ __forceinline__ uint32_t dq_done() const { return bar(X + 7); }
+  __device__ __forceinline__ uint32_t drain() const { return bar(X + 8); }
+};
+
+// One dQ work item: a 128-query tile of one (batch, head) and the number of
+// key tiles any of its rows sees.  Each role computes it alike.
+struct DqItem {
+  int bh, q0, kv_limit, n_kv;
+};
+__device__ __forceinline__ DqItem dq_item(const BwdParams& p, const WorkList& w, int k) {
+  int bh, qt;  // units of a head: its query tiles, the last one heaviest under a causal mask
+  wl_item(w, k, p.n_qt, true, bh, qt);
+  DqItem g;
+  g.bh = bh;
+  g.q0 = qt * DqLayout::BM;
+  g.kv_limit = p.Nk;
+  if (p.kv_len) g.kv_limit = min(p.Nk, max(0, p.kv_len[bh / p.H]));
+  int kl = g.kv_limit;  // keys < kl can be visible to some row of the tile
+  // causal: key c is visible to query row i iff c < i + qoff
+  if (p.causal) kl = min(kl, min(g.q0 + DqLayout::BM, p.N) - 1 + p.qoff);
+  g.n_kv = kl > 0 ? (kl + DqLayout::BN - 1) / DqLayout::BN : 0;
+  return g;
+}
+
+__global__ void __launch_bounds__(384, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_do, const BwdParams p, const __grid_constant__ WorkList sc) {
+  using L = DqLayout;
+  constexpr int D = L::D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  volatile int* issued_do = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);  // dO loads issued
+  volatile int* issued_k = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);   // K tiles issued
+  volatile int* issued_v = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);   // V tiles issued
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    const DqSmem sm(smem_u32_fresh(smem_raw));
+    mbar_init(sm.do_full(), 1);
+    mbar_init(sm.do_free(), 1);
+    for (int s = 0; s < L::NK; ++s) {
+      mbar_init(sm.k_full(s), 1);
+      mbar_init(sm.k_empty(s), 1);
+    }
+    for (int s = 0; s < L::NV; ++s) {
+      mbar_init(sm.v_full(s), 1);
+      mbar_init(sm.v_empty(s), 1);
+    }
+    mbar_init(sm.q_ready(), 256);
+    mbar_init(sm.s_full(), 1);
+    mbar_init(sm.s_free(), 256);
+    mbar_init(sm.dp_full(), 1);
+    mbar_init(sm.dp_free(), 256);
+    mbar_init(sm.ds_full(), 256);
+    mbar_init(sm.ds_free(), 1);
+    mbar_init(sm.dq_done(), 1);
+    mbar_init(sm.drain(), 1);
+    *abort_flag = 0;
+    *issued_do = 0;
+    *issued_k = 0;
+    *issued_v = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
+
+  if (warp == 0) {
+    reg_lower<BWD_REGS_LOW>();
+    const DqSmem sm(smem_u32_fresh(smem_raw));
+    const uint32_t sbase = sm.base;
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
+    // ------------------------------------------------------------ producer --
+    // Per item: dO (once the previous item's dP products have run), then K_j and
+    // V_j of every key tile.  J counts key tiles over all of the CTA's items
+    // (ring slots and barrier phases).
+    if (lane == 0) {
+      int J = 0, nq = 0;
+      bool go = true;
+      for (int k = 0; go && k < n_items; ++k) {
+        const DqItem g = dq_item(p, sc, k);
+        if (g.n_kv == 0) continue;
+        if (nq > 0 && !mbar_wait(sm.do_free(), (nq - 1) & 1, wc, ST_BWD_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(sm.do_full(), L::TILE);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(sbase + L::OFF_DO + kb * L::COLBLK, &tm_do, sm.do_full(), kb * 64, g.q0, g.bh);
+        *issued_do = ++nq;
+        for (int j = 0; j < g.n_kv; ++j, ++J) {
+          if (p.inject == 3 && J == 1) {  // test hook: starve the consumers after the first key tile
+            go = false;
+            break;
+          }
+          const int ks = J % L::NK, vs = J % L::NV;
+          if (J >= L::NK && !mbar_wait(sm.k_empty(ks), ((J / L::NK) - 1) & 1, wc, ST_BWD_TIMEOUT_EMPTY)) {
+            go = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sm.k_full(ks), L::TILE);
+#pragma unroll
+          for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(sbase + L::OFF_K + ks * L::TILE + kb * L::COLBLK, &tm_k, sm.k_full(ks), kb * 64,
+                        j * L::BN, g.bh);
+          *issued_k = J + 1;
+          if (J >= L::NV && !mbar_wait(sm.v_empty(vs), ((J / L::NV) - 1) & 1, wc, ST_BWD_TIMEOUT_EMPTY)) {
+            go = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sm.v_full(vs), L::TILE);
+#pragma unroll
+          for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(sbase + L::OFF_V + vs * L::TILE + kb * L::COLBLK, &tm_v, sm.v_full(vs), kb * 64,
+                        j * L::BN, g.bh);
+          *issued_v = J + 1;
+        }
+      }
+    }
+    tc_fence_before();
+    cta_bar_sync<384>();
+    if (lane == 0 && *abort_flag) {
+      // an aborted CTA may not exit while copies it issued are still landing
+      const int nq = *issued_do, nk = *issued_k, nv = *issued_v;
+      bool drained = nq == 0 || mbar_wait_drain(sm.do_full(), (nq - 1) & 1, DRAIN_NS);
+      for (int j = max(0, nk - L::NK); j < nk; ++j)
+        drained &= mbar_wait_drain(sm.k_full(j % L::NK), (j / L::NK) & 1, DRAIN_NS);
+      for (int j = max(0, nv - L::NV); j < nv; ++j)
+        drained &= mbar_wait_drain(sm.v_full(j % L::NV), (j / L::NV) & 1, DRAIN_NS);
+      if (!drained) atomicOr(p.status, ST_DRAIN);
+    }
+  } else if (warp == 1) {
+    reg_lower<BWD_REGS_LOW>();
+    const DqSmem sm(smem_u32_fresh(smem_raw));
+    const uint32_t sbase = sm.base;
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // ---------------------------------------------------------- MMA issuer --
+    // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(L::BM, L::BN, false, false);  // Q K^T, dO V^T
+    constexpr uint32_t IDESC_Q = idesc_bf16_f32(L::BM, D, true, false);       // dS K
+    // Descriptors of the operand bases; an operand at byte offset `off` from a
+    // base is that descriptor plus off >> 4 (the start-address field is the
+    // low 14 bits and every shared address here is below 2^18, so no carry).
+    const uint64_t d_do = sdesc_sw128(sbase + L::OFF_DO, 16, 1024);  // K-major: dO, K, V
+    const uint64_t d_k = sdesc_sw128(sbase + L::OFF_K, 16, 1024);
+    const uint64_t d_v = sdesc_sw128(sbase + L::OFF_V, 16, 1024);
+    const uint64_t m_k = sdesc_sw128(sbase + L::OFF_K, L::COLBLK, 1024);  // MN-major: K
+    constexpr uint32_t TILE16 = L::TILE >> 4;
+
+    // S_j = Q K_j^T of CTA-wide key tile G, once the warps have read S_{G-1} and
+    // K_j has landed.  A = Q from tensor memory (16 head-dim columns = 8 TMEM
+    // columns per step), B = K_j K-major.
+    auto issue_s = [&](int G) -> bool {
+      const int ks = G % L::NK;
+      if ((G >= 1 && !mbar_wait_w(sm.s_free(), (G - 1) & 1, wc, ST_BWD_TIMEOUT_S)) ||
+          !mbar_wait_w(sm.k_full(ks), (G / L::NK) & 1, wc, ST_BWD_TIMEOUT_KV))
+        return false;
+      tc_fence_after();
+      umma_ts_c_k8(tmem + L::TM_S, tmem + L::TM_Q, d_k + ks * TILE16, IDESC_S, 0u);
+      umma_commit_w(sm.s_full());
+      return true;
+    };
+    // dP_j = dO V_j^T, once the warps have read dP_{G-1} and V_j has landed; the
+    // commit frees V_j's slot
+    auto issue_dp = [&](int G) -> bool {
+      const int vs = G % L::NV;
+      if ((G >= 1 && !mbar_wait_w(sm.dp_free(), (G - 1) & 1, wc, ST_BWD_TIMEOUT_DP)) ||
+          !mbar_wait_w(sm.v_full(vs), (G / L::NV) & 1, wc, ST_BWD_TIMEOUT_KV))
+        return false;
+      tc_fence_after();
+      umma_ss_k8(tmem + L::TM_DP, d_do, d_v + vs * TILE16, IDESC_S, 0u);
+      umma_commit_w(sm.dp_full());
+      umma_commit_w(sm.v_empty(vs));
+      return true;
+    };
+    int G0 = 0, nq = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < n_items; ++k) {
+      const int n = dq_item(p, sc, k).n_kv;
+      if (n == 0) continue;
+      ok = mbar_wait_w(sm.q_ready(), nq & 1, wc, ST_BWD_TIMEOUT_Q) && issue_s(G0) &&
+           mbar_wait_w(sm.do_full(), nq & 1, wc, ST_BWD_TIMEOUT_Q) && issue_dp(G0);
+      if (!ok) break;
+      if (n == 1) umma_commit_w(sm.do_free());  // no later product of the item reads dO
+      for (int j = 0; j < n; ++j) {
+        const int G = G0 + j;
+        if (j + 1 < n && !(issue_s(G + 1) && issue_dp(G + 1))) {
+          ok = false;
+          break;
+        }
+        if (j + 2 == n) umma_commit_w(sm.do_free());  // dP_{n-1} is issued
+        // dQ (+)= dS_j K_j.  A = dS_j from the dS columns (keys 0-63 in the first
+        // 32, 64-127 in the last 32, bf16 pairs); B = K_j MN-major, 16 keys = 2 KB
+        // per step.  dQ starts over at an item's first key tile: the warpgroups
+        // store an item's first dS only after writing out the previous item's dQ.
+        // The commits free the dS columns and K_j's slot (S_j read it before).
+        if (!mbar_wait_w(sm.ds_full(), G & 1, wc, ST_BWD_TIMEOUT_DS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ks = G % L::NK;
+        umma_ts_c_mn8(tmem + L::TM_DQ, tmem + L::TM_DS, m_k + ks * TILE16, IDESC_Q, j > 0 ? 1u : 0u);
+        umma_commit_w(sm.ds_free());
+        umma_commit_w(sm.k_empty(ks));
+      }
+      if (!ok) break;
+      umma_commit_w(sm.dq_done());  // dQ of the item is complete
+      G0 += n;
+      ++nq;
+    }
+    // nothing may be in flight on the tensor cores when the CTA frees TMEM
+    umma_commit_w(sm.drain());
+    if (!mbar_wait_drain(sm.drain(), 0, DRAIN_NS) && lane == 0) atomicOr(p.status, ST_DRAIN);
+    tc_fence_before();
+    cta_bar_sync<384>();
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TM_COLS);
+  } else if (warp >= 4) {
+    reg_raise<BWD_REGS_HIGH>();
+    const DqSmem sm(smem_u32_fresh(smem_raw));
+    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+    const int n_items = wl_count(sc);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // ---------------------------------------------------- elementwise WGs --
+    // Both warpgroups take every key tile: warpgroup h owns keys [64 h, 64 h +
+    // 64) of it and head-dim columns [64 h, 64 h + 64) of Q and dQ.  Thread r is
+    // query row r (TMEM lane r).
+    const int h = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t sc2 = f2_pack(p.scale, p.scale);
+    // the next item (from k on) whose tile sees some key, or n_items
+    auto next_with_keys = [&](int k) -> int {
+      while (k < n_items && dq_item(p, sc, k).n_kv == 0) ++k;
+      return k;
+    };
+    // this thread's half of a Q row (64 bf16, 8 x 16 bytes); zeros past N
+    auto load_q = [&](int k, uint4 (&qv)[8]) {
+      const DqItem g = dq_item(p, sc, k);
+      const int qi = g.q0 + r;
+      if (qi < p.N) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(g.bh) * p.N + qi) * D + h * 64);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qv[i] = src[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qv[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    // ... into this warpgroup's Q columns, then arrive on q_ready
+    auto store_q = [&](uint4 (&qv)[8]) {
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        w[4 * i] = qv[i].x;
+        w[4 * i + 1] = qv[i].y;
+        w[4 * i + 2] = qv[i].z;
+        w[4 * i + 3] = qv[i].w;
+      }
+      FA_TMEM_ST32(lane_base + L::TM_Q + h * 32, w);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sm.q_ready());
+    };
+    bool ok = true;
+    int G0 = 0, nq = 0;
+    {
+      const int k0 = next_with_keys(0);
+      if (k0 < n_items) {
+        uint4 qv[8];
+        load_q(k0, qv);
+        store_q(qv);
+      }
+    }
+    for (int k = 0; ok && k < n_items; ++k) {
+      const DqItem g = dq_item(p, sc, k);
+      const int n = g.n_kv;
+      const int qi = g.q0 + r;
+      // the workspace rows are padded to a multiple of 128 (nl = -inf past N)
+      const size_t ws = static_cast<size_t>(g.bh) * p.Np + qi;
+      const float nl = n > 0 ? p.nl[ws] : 0.f, nd = n > 0 ? p.nd[ws] : 0.f;
+      const uint64_t nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
+      // keys of this row from kmax on are masked (padding or, causal, key >= qi + qoff)
+      const int kmax = p.causal ? min(g.kv_limit, qi + p.qoff) : g.kv_limit;
+      const int kq = n > 0 ? next_with_keys(k + 1) : n_items;  // the item whose Q comes next
+      for (int j = 0; j < n; ++j) {
+        const int G = G0 + j;
+        const bool q_next = j + 1 == n && kq < n_items;
+        uint4 qv[8];
+        if (q_next) load_q(kq, qv);  // issued early, stored once the last S is read
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.s_full(), G & 1, wc, ST_BWD_TIMEOUT_S))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float pr[64];  // P_j of this thread's query row over the half's 64 keys
+        {
+          uint32_t sr[64];
+          const uint32_t s_col = lane_base + L::TM_S + h * 64;
+          FA_TMEM_LD32(s_col, sr);
+          FA_TMEM_LD32(s_col + 32, sr + 32);
+          tmem_wait_ld();
+          FA_REG_FENCE32(sr);
+          FA_REG_FENCE32(sr + 32);
+          tc_fence_before();
+          mbar_arrive(sm.s_free());  // the scores are in registers: S_{j+1} may overwrite them
+          // the item's last S has run, so nothing reads Q any more: the next
+          // item's Q goes in now, and its first products can start meanwhile
+          if (q_next) store_q(qv);
+          const int wmax = kmax - (j * L::BN + h * 64);  // columns w >= wmax are masked
+          if (__any_sync(0xffffffffu, wmax < 64)) {
+#pragma unroll
+            for (int w = 0; w < 64; ++w)
+              if (w >= wmax) sr[w] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int w = 0; w < 64; w += 2) {
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[w]), __uint_as_float(sr[w + 1])), sl2, nl2);
+            constexpr int E = FA_BWD_EXP2_FMA_EVERY > 0 ? FA_BWD_EXP2_FMA_EVERY : 1;
+            if (FA_BWD_EXP2_FMA_EVERY > 0 && (w / 2 + 1) % E == 0) {
+              f2_unpack(exp2_fma2(x2), pr[w], pr[w + 1]);  // FMA pipe
+            } else {
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              pr[w] = ex2_approx(x0);
+              pr[w + 1] = ex2_approx(x1);
+            }
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.dp_full(), G & 1, wc, ST_BWD_TIMEOUT_DP))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dsk[32];
+        {
+          uint32_t dpr[64];
+          const uint32_t dp_col = lane_base + L::TM_DP + h * 64;
+          FA_TMEM_LD32(dp_col, dpr);
+          FA_TMEM_LD32(dp_col + 32, dpr + 32);
+          tmem_wait_ld();
+          FA_REG_FENCE32(dpr);
+          FA_REG_FENCE32(dpr + 32);
+          tc_fence_before();
+          mbar_arrive(sm.dp_free());  // dP_{j+1} may overwrite it
+#pragma unroll
+          for (int w = 0; w < 64; w += 2) {
+            // dS = P (dP scale - D scale)
+            const uint64_t gr =
+                f2_mul(f2_fma(f2_pack(__uint_as_float(dpr[w]), __uint_as_float(dpr[w + 1])), sc2, nd2),
+                       f2_pack(pr[w], pr[w + 1]));
+            float g0, g1;
+            f2_unpack(gr, g0, g1);
+            dsk[w / 2] = pack_bf16x2(g0, g1);
+          }
+        }
+        // dS_j as the dQ product's A operand, once dQ_{j-1} has read dS_{j-1}
+        if (!__all_sync(0xffffffffu, G == 0 || mbar_wait(sm.ds_free(), (G - 1) & 1, wc, ST_BWD_TIMEOUT_DS))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        FA_TMEM_ST32(lane_base + L::TM_DS + h * 32, dsk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sm.ds_full());
+      }
+
+      // ---------------------------------------------------------- epilogue --
+      // warpgroup h writes dQ columns [64 h, 64 h + 64) of row qi (TMEM lane r);
+      // a tile that sees no key gets zeros
+      if (ok && n > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.dq_done(), nq & 1, wc, ST_BWD_TIMEOUT_DQ)))
+        ok = false;
+      if (ok) {
+        tc_fence_after();
+        float* out = p.dq + (static_cast<size_t>(g.bh) * p.N + qi) * D + h * 64;
+        const uint32_t col = lane_base + L::TM_DQ + h * 64;
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          uint32_t v[32];
+          if (n > 0) {
+            FA_TMEM_LD32(col + cb * 32, v);
+            tmem_wait_ld();
+            FA_REG_FENCE32(v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (qi < p.N) {
+            float4* o4 = reinterpret_cast<float4*>(out + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+        // the next item's first dQ product overwrites dQ only after these
+        // warpgroups' ds_full for it, i.e. after these loads
+        tc_fence_before();
+      }
+      if (n > 0) {
+        G0 += n;
+        ++nq;
+      }
+    }
+    tc_fence_before();
+    cta_bar_sync<384>();
+  } else {
+    reg_lower<BWD_REGS_LOW>();  // warps 2-3: no role
+    cta_bar_sync<384>();
+  }
+  // Launched to overlap the tail of the dK/dV kernel: this grid completes only
+  // after that one has, so that work queued behind it on the stream sees dK and
+  // dV as well as dQ.
+  if (threadIdx.x == 0) griddep_wait();
+}
+
+}  // namespace fa

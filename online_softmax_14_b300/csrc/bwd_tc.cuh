@@ -1,4 +1,6 @@
-// BFloat16 attention backward on the 5th-generation tensor cores (tcgen05, sm_103a).
+// BFloat16 attention backward on the 5th-generation tensor cores (tcgen05, sm_103a):
+// the row preprocess and the per-key-tile kernel for dK and dV.  dQ comes from
+// bwd_dq_kernel (bwd_dq.cuh).
 //
 // The backward pass recomputes the scores and probabilities instead of reading a
 // stored N x N matrix ("Question bank -- Flash attention and efficient
@@ -10,57 +12,53 @@
 // P is rebuilt from the forward's lse: P_ij = exp(scale S_ij - lse_i), which is
 // already normalised, so no second softmax pass is needed.
 //
-// Two kernels:
+// Why dQ has a kernel of its own.  dQ sums over key tiles, dK and dV over query
+// tiles; one CTA can accumulate only one side in tensor memory.  Adding the other
+// side's partial tiles into device memory (a tiled reduce-add per 128 x 128 tile)
+// runs on the SM's path for reductions, which measured about 24 bytes per cycle
+// per SM on B300 whatever issues them: 64 KB of dQ per tile needs at least 2700
+// cycles, more than the tile's products.  So the per-key-tile kernel here makes
+// no dQ, and bwd_dq_kernel, per query tile, recomputes S and dP and accumulates
+// dQ in tensor memory: seven products per tile instead of five, no reductions,
+// and a deterministic dQ.
+//
+// Kernels:
 //  * bwd_preprocess_kernel -- nl_i = -lse_i log2(e) and nd_i = -D_i scale into
 //    the workspace (row stride Np = N rounded up to 128; padding rows get nl =
-//    -inf, so that their probabilities are exactly 0, and nd = 0), and zeroes dQ.
-//    With them P^T = 2^(S^T scale log2e + nl) and dS^T = P^T (dP^T scale + nd)
-//    take one packed FMA (and one packed multiply) per pair of entries.
-//  * bwd_bf16_tc_kernel -- one CTA per (batch, head, 128-key tile).  K and V stay
-//    in shared memory; the CTA streams 128-query tiles (Q_t with its nl_t and
-//    nd_t rows, and dO_t) through a 2-stage TMA ring and, per tile t, runs five
-//    MMAs (128 x 128 x 128 each):
+//    -inf, so that their probabilities are exactly 0, and nd = 0).  With them
+//    P = 2^(S scale log2e + nl) and dS = P (dP scale + nd) take one packed FMA
+//    (and one packed multiply) per pair of entries.
+//  * bwd_dkdv_kernel -- persistent; an item is (batch*head, 128-key tile).  K and
+//    V stay in shared memory; the CTA streams 128-query tiles (Q_t with its nl_t
+//    and nd_t rows, and dO_t) through a 2-stage TMA ring and, per tile t, runs
+//    four MMAs (128 x 128 x 128 each):
 //       MMA1  S^T_t  = K Q_t^T            (A = K, B = Q_t, both from SMEM)
 //       MMA2  dP^T_t = V dO_t^T           (A = V, B = dO_t)
 //       MMA3  dV    += P^T_t dO_t          (A = P^T from TMEM, B = dO_t MN-major)
 //       MMA4  dK    += dS^T_t Q_t          (A = dS^T from TMEM, B = Q_t MN-major)
-//       MMA5  dQ^T_t = K^T dS_t            (A = K MN-major, B = dS^T MN-major, SMEM)
-//    issued as MMA3_t, MMA4_t, MMA5_t, MMA1_{t+1}, MMA2_{t+1}.  dS carries the
-//    factor `scale`, so dK and dQ need no further scaling.
-//    dQ^T_t is staged row-major in shared memory -- the query half 0-63 in dO_t's
-//    buffer, the half 64-127 in Q_t's buffer -- and added into global dQ with two
-//    tiled TMA reduce-adds (cp.reduce.async.bulk.tensor .add.f32), which skip the
-//    rows past N.  The producer refills those buffers only after the reduce-adds
-//    have read them.
-//    Why this order: the staging needs 64 KB of shared memory that is free for
-//    as long as a reduce-add reads it (about as long as two products take), and
-//    only the tile's own Q and dO buffers qualify -- provided S^T_{t+1} = K
-//    Q_{t+1}^T is not issued early (then Q_{t+2} would be needed before the
-//    reduce-add has released Q_t's buffer).  The dS buffer, which MMA5_t reads,
-//    is thus never used for staging, and the next tile's dS^T is not held up by
-//    a reduce-add.  While the elementwise warps form P^T_{t+1}, the tensor cores
-//    run MMA2_{t+1}; while they form dS^T_{t+1}, MMA3_{t+1}.
+//    issued as MMA3_t, MMA1_{t+1}, MMA4_t, MMA2_{t+1}: each product overwrites a
+//    tensor-memory region only after the product reading it was issued, and the
+//    tensor cores run in issue order.  While the elementwise warps form dS^T_t,
+//    the tensor cores run MMA3_t and MMA1_{t+1}; while they form P^T_{t+1},
+//    MMA4_t and MMA2_{t+1}.  dS carries the factor `scale`, so dK needs no
+//    further scaling.
 //
 // Roles (384 threads):
-//   warp 0     TMA producer: K, V once; then Q_t + nl_t + nd_t and dO_t into the
-//              ring (separate full / empty barriers for Q and dO).
+//   warp 0     TMA producer: per item K, V; then Q_t + nl_t + nd_t and dO_t into
+//              the ring (separate full / empty barriers for Q and dO).
 //   warp 1     MMA issuer (lane 0 of the converged warp) and tensor-memory owner.
-//   warp 2     dQ reducer: issues the reduce-adds once a half is staged and
-//              hands the buffers back when the copies have read them.
-//   warp 3     no role.
+//   warps 2-3  no role.
 //   warps 4-7  elementwise warpgroup 0, query columns 0-63 of every tile;
 //   warps 8-11 elementwise warpgroup 1, query columns 64-127.
 //              Thread r owns key row r (TMEM lane r) of S^T and dP^T:
 //                P^T = 2^(S^T scale log2e + nl) with the causal / padding mask,
 //                written back to TMEM as bf16 (aliasing S^T); then
-//                dS^T = P^T (dP^T scale + nd) -> bf16, into TMEM (aliasing
-//                dP^T, for MMA4) and 128B-swizzled into SMEM (for MMA5); and, as
-//                TMEM lane r of dQ^T, stages head-dim column r of its 64 dQ rows.
-//              At the end warpgroup 0 writes dV and warpgroup 1 writes dK.
+//                dS^T = P^T (dP^T scale + nd) -> bf16, into TMEM (aliasing dP^T).
+//              At the end of an item warpgroup 0 writes dV and warpgroup 1 dK.
 //
 // Tensor memory (512 columns, f32 unless noted):
 //   [0,128)   S^T_t, then P^T_t (bf16: queries 0-63 in [0,32), 64-127 in [64,96))
-//   [128,256) dP^T_t, then dS^T_t (bf16, laid out like P^T), then dQ^T_t
+//   [128,256) dP^T_t, then dS^T_t (bf16, laid out like P^T)
 //   [256,384) dV   [384,512) dK
 //
 // Every wait is bounded, as in the forward kernel: a wait that runs out records
@@ -86,15 +84,13 @@ enum : unsigned {
   ST_BWD_TIMEOUT_DP = 1u << 12,
   ST_BWD_TIMEOUT_DS = 1u << 13,
   ST_BWD_TIMEOUT_DQ = 1u << 14,
-  ST_BWD_TIMEOUT_DQE = 1u << 15,
   ST_BWD_TIMEOUT_EMPTY = 1u << 16,
   ST_BWD_TIMEOUT_DONE = 1u << 17,
-  ST_BWD_TIMEOUT_RED = 1u << 18,
   ST_BWD_SMEM_ALIGN = 1u << 19,   // dynamic shared memory base not aligned enough (kernel did nothing)
 };
 
 // Register shares (launch: 384 threads x 168): warps 0-3 (producer, MMA issuer,
-// reducer, idle) keep BWD_REGS_LOW, the elementwise warpgroups get BWD_REGS_HIGH.
+// idle) keep BWD_REGS_LOW, the elementwise warpgroups get BWD_REGS_HIGH.
 constexpr uint32_t BWD_REGS_LOW = 56, BWD_REGS_HIGH = 216;
 static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= 384 * 168, "register split exceeds the launch");
 
@@ -102,88 +98,88 @@ struct BwdPreParams {
   const __nv_bfloat16* o;   // [BH, N, D]
   const __nv_bfloat16* dO;  // [BH, N, D]
   const float* lse;         // [BH, N]
-  float* dq;                // [BH, N, D], zeroed here
   float* nl;                // workspace [BH, Np]: -lse log2(e)
   float* nd;                // workspace [BH, Np]: -D scale
   int BH, N, Np;
   float scale;
 };
 
-// One warp per row: D = sum_c dO_c O_c (f32); nl = -lse log2(e) (-inf where
-// lse = -inf or the row is padding); nd = -D scale; dq row = 0.  Grid: BH * Np / 64
-// blocks of 256 threads, 8 rows per warp.
+// D = sum_c dO_c O_c (f32) per row; nl = -lse log2(e) (-inf where lse = -inf
+// or the row is padding); nd = -D scale.  Half a warp per row (16 lanes x 8
+// elements, 16-byte loads); a warp takes 8 rows and issues all of its loads
+// before the first reduction.  Grid: BH * Np / 64 blocks of 256 threads.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p) {
-  constexpr int EPL = D / 32;  // elements per lane
+  static_assert(D == 128, "16 lanes x 8 elements per row");
   const int chunks = p.Np / 64;
   const int bh = static_cast<int>(blockIdx.x) / chunks;
-  const int row0 = (static_cast<int>(blockIdx.x) % chunks) * 64 + (threadIdx.x >> 5) * 8;
-  const int lane = threadIdx.x & 31;
-  for (int rr = 0; rr < 8; ++rr) {
-    const int row = row0 + rr;
-    const size_t ws = static_cast<size_t>(bh) * p.Np + row;
-    if (row >= p.N) {
-      if (lane == 0) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+  const int row0 = (static_cast<int>(blockIdx.x) % chunks) * 64 + (threadIdx.x >> 5) * 8 + half;
+  uint4 a[4], g[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int row = row0 + 2 * s;
+    if (row < p.N) {
+      const size_t base = (static_cast<size_t>(bh) * p.N + row) * D + hl * 8;
+      a[s] = *reinterpret_cast<const uint4*>(p.o + base);
+      g[s] = *reinterpret_cast<const uint4*>(p.dO + base);
+    } else {
+      a[s] = make_uint4(0u, 0u, 0u, 0u);
+      g[s] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[s]);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[s]);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 af = __bfloat1622float2(a2[i]), gf = __bfloat1622float2(g2[i]);
+      acc = fmaf(af.x, gf.x, acc);
+      acc = fmaf(af.y, gf.y, acc);
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);  // within the half
+    const int row = row0 + 2 * s;
+    if (hl == 0) {
+      const size_t ws = static_cast<size_t>(bh) * p.Np + row;
+      if (row < p.N) {
+        const float l = p.lse[static_cast<size_t>(bh) * p.N + row];
+        p.nl[ws] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+        p.nd[ws] = -acc * p.scale;
+      } else {
         p.nl[ws] = -INFINITY;
         p.nd[ws] = 0.f;
       }
-      continue;
-    }
-    const size_t base = (static_cast<size_t>(bh) * p.N + row) * D + lane * EPL;
-    float acc = 0.f;
-    if constexpr (EPL == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(p.o + base);
-      const uint2 g = *reinterpret_cast<const uint2*>(p.dO + base);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float2 af = __bfloat1622float2(a2[i]), gf = __bfloat1622float2(g2[i]);
-        acc = fmaf(af.x, gf.x, acc);
-        acc = fmaf(af.y, gf.y, acc);
-      }
-      *reinterpret_cast<float4*>(p.dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(p.o + base);
-      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(p.dO + base);
-      const float2 af = __bfloat1622float2(a), gf = __bfloat1622float2(g);
-      acc = fmaf(af.x, gf.x, fmaf(af.y, gf.y, 0.f));
-      *reinterpret_cast<float2*>(p.dq + base) = make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      const float l = p.lse[static_cast<size_t>(bh) * p.N + row];
-      p.nl[ws] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
-      p.nd[ws] = -acc * p.scale;
     }
   }
 }
 
 struct BwdParams {
-  float* dq;                // [BH, N, D], accumulated by tiled reduce-adds (tensor map tm_dq)
+  float* dq;                // [BH, N, D], written once per row by bwd_dq_kernel
   float* dk;                // [BH, Nk, D]
   float* dv;                // [BH, Nk, D]
   const float* nl;          // [BH, Np]: -lse log2(e)
   const float* nd;          // [BH, Np]: -D scale
+  const __nv_bfloat16* q;   // [BH, N, D]: the dQ kernel copies its rows into tensor memory
   const int* kv_len;        // [B] or null
   int BH, H, N, Np;         // N queries per head
   int Nk;                   // keys per head
-  int n_kt;                 // key tiles per head
+  int n_qt, n_kt;           // query tiles, key tiles per head
   float scale;              // score multiplier
   float scale_log2;         // scale * log2(e)
   int causal;               // 0 none, else key k visible to query row i iff k < i + qoff
   int qoff;                 // (Nk - N) + 1 (causal 1) or (Nk - N) (causal 2, strict)
   unsigned* status;
   unsigned long long timeout_ns;
-  int inject;               // test hook: 2 = producer stops after the first Q / dO tile
+  int inject;               // test hook: 2 = the dK/dV producer stops after the first Q / dO tile
 };
-
 
 template <int STAGES>
 struct BwdLayout {
   static constexpr int D = 128;
-  static constexpr int BN = 128;                   // keys per CTA
+  static constexpr int BN = 128;                   // keys per item
   static constexpr int BM = 128;                   // queries per tile
   static constexpr int KB = D / 64;                // 128-byte column blocks
   static constexpr int COLBLK = 128 * 128;         // 16 KB: 128 rows x 128 bytes
@@ -192,23 +188,22 @@ struct BwdLayout {
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
-  static constexpr int OFF_DS = OFF_DO + STAGES * TILE;  // dS^T: 2 column blocks of 64 queries
-  static constexpr int OFF_STAT = OFF_DS + 2 * COLBLK;   // per stage: nl[128], nd[128]
+  static constexpr int OFF_STAT = OFF_DO + STAGES * TILE;  // per stage: nl[128], nd[128]
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
-  // barriers: kv_full, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full, dp_full,
-  //           ds_full, dq_full, dq_empty, red_ready[2], dkv_done, drain, q_issued, kv_free
-  static constexpr int NBAR = 1 + 4 * STAGES + 6 + 2 + 4;
+  // barriers: kv_full, kv_free, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full,
+  //           dp_full, ds_full, dkv_done, drain
+  static constexpr int NBAR = 2 + 4 * STAGES + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int USED = OFF_MISC + 32;
-  static constexpr int BYTES = 232448;             // the whole per-CTA budget
-  static constexpr int SLACK = BYTES - USED;        // room to align the base up to 1024 bytes
-  // S^T, then P^T (bf16, in each half's own columns), | dP^T, then dQ^T | dV | dK
+  static constexpr int BYTES = OFF_MISC + 32 + 1024;  // room to align the base up to 1024 bytes
+  // S^T, then P^T (bf16, in each half's own columns) | dP^T, then dS^T | dV | dK
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
-  static_assert(SLACK >= 0, "shared memory budget");
+  static_assert(BYTES <= 232448, "shared memory budget");
 };
 
-// Shared-memory addresses (32-bit) of the backward kernel's buffers and
-// barriers, from the 1024-aligned base of its dynamic shared memory.
+// Shared-memory addresses (32-bit) of the dK/dV kernel's buffers and barriers,
+// from the 1024-aligned base of its dynamic shared memory.  Each role builds its
+// own copy (from smem_u32_fresh) after changing its register budget, so that no
+// address is held across that change.
 template <int STAGES>
 struct BwdSmem {
   using L = BwdLayout<STAGES>;
@@ -216,28 +211,21 @@ struct BwdSmem {
   __device__ __forceinline__ explicit BwdSmem(uint32_t raw) : base((raw + 1023u) & ~1023u) {}
   __device__ __forceinline__ uint32_t bar(int i) const { return base + L::OFF_BAR + 8 * i; }
   __device__ __forceinline__ uint32_t kv_full() const { return bar(0); }
-  __device__ __forceinline__ uint32_t q_full(int s) const { return bar(1 + s); }  // Q_t, nl_t, nd_t landed
-  __device__ __forceinline__ uint32_t do_full(int s) const { return bar(1 + STAGES + s); }  // dO_t landed
-  // the dQ_t half staged in Q_t's / dO_t's buffer has been read
-  __device__ __forceinline__ uint32_t q_empty(int s) const { return bar(1 + 2 * STAGES + s); }
-  __device__ __forceinline__ uint32_t do_empty(int s) const { return bar(1 + 3 * STAGES + s); }
-  __device__ __forceinline__ uint32_t s_full() const { return bar(1 + 4 * STAGES); }
-  __device__ __forceinline__ uint32_t p_full() const { return bar(2 + 4 * STAGES); }
-  __device__ __forceinline__ uint32_t dp_full() const { return bar(3 + 4 * STAGES); }
-  __device__ __forceinline__ uint32_t ds_full() const { return bar(4 + 4 * STAGES); }
-  __device__ __forceinline__ uint32_t dq_full() const { return bar(5 + 4 * STAGES); }
-  __device__ __forceinline__ uint32_t dq_empty() const { return bar(6 + 4 * STAGES); }
-  // warpgroup h has staged its dQ_t half
-  __device__ __forceinline__ uint32_t red_ready(int h) const { return bar(7 + 4 * STAGES + h); }
-  __device__ __forceinline__ uint32_t dkv_done() const { return bar(9 + 4 * STAGES); }
-  __device__ __forceinline__ uint32_t drain() const { return bar(10 + 4 * STAGES); }
-  // the producer has issued the load of Q_t (one phase per query tile)
-  __device__ __forceinline__ uint32_t q_issued() const { return bar(11 + 4 * STAGES); }
-  // every product of an item that reads K or V has run (one phase per item)
-  __device__ __forceinline__ uint32_t kv_free() const { return bar(12 + 4 * STAGES); }
+  // every product of an item that reads K or V has been issued (one phase per item)
+  __device__ __forceinline__ uint32_t kv_free() const { return bar(1); }
+  __device__ __forceinline__ uint32_t q_full(int s) const { return bar(2 + s); }  // Q_t, nl_t, nd_t landed
+  __device__ __forceinline__ uint32_t do_full(int s) const { return bar(2 + STAGES + s); }
+  __device__ __forceinline__ uint32_t q_empty(int s) const { return bar(2 + 2 * STAGES + s); }  // MMA4_t done
+  __device__ __forceinline__ uint32_t do_empty(int s) const { return bar(2 + 3 * STAGES + s); }  // MMA3_t done
+  __device__ __forceinline__ uint32_t s_full() const { return bar(2 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t p_full() const { return bar(3 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t dp_full() const { return bar(4 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t ds_full() const { return bar(5 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t dkv_done() const { return bar(6 + 4 * STAGES); }
+  __device__ __forceinline__ uint32_t drain() const { return bar(7 + 4 * STAGES); }
 };
 
-// One backward work item: a 128-key tile of one (batch, head), and the range of
+// One dK/dV work item: a 128-key tile of one (batch, head), and the range of
 // query tiles that see it (under a causal mask, from the tile holding the key
 // tile's first visible query on).  Each role computes it alike.
 struct BwdItem {
@@ -252,31 +240,20 @@ __device__ __forceinline__ BwdItem bwd_item(const Params& p, const WorkList& w, 
   g.k0 = kt * BN;
   g.kv_limit = p.Nk;
   if (p.kv_len) g.kv_limit = min(p.Nk, max(0, p.kv_len[bh / p.H]));
-  const int n_qt = (p.N + BM - 1) / BM;
   // causal: key k0 is visible to query rows i >= k0 - qoff + 1
   g.i0 = p.causal ? max(0, g.k0 - p.qoff + 1) / BM : 0;
-  g.n_it = (g.k0 < g.kv_limit && g.i0 < n_qt) ? n_qt - g.i0 : 0;
+  g.n_it = (g.k0 < g.kv_limit && g.i0 < p.n_qt) ? p.n_qt - g.i0 : 0;
   return g;
 }
 
 template <int STAGES>
 __global__ void __launch_bounds__(384, 1)
-    bwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p,
-                       const __grid_constant__ WorkList sc) {
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p, const __grid_constant__ WorkList sc) {
   using L = BwdLayout<STAGES>;
   constexpr int D = L::D;
   extern __shared__ uint8_t smem_raw[];
-  {
-    // the layout fills the budget but for SLACK bytes: the base must be aligned
-    // to within SLACK of 1024 bytes (it is 1024-aligned in practice)
-    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-    if (pad > static_cast<uint32_t>(L::SLACK)) {
-      if (threadIdx.x == 0) atomicOr(p.status, ST_BWD_SMEM_ALIGN);
-      return;
-    }
-  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
@@ -284,9 +261,13 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* issued_do = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);
   volatile int* issued_kv = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);  // K/V loads issued
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the dQ kernel that follows reads nothing this kernel writes: its CTAs may
+  // take each SM as soon as this kernel's CTA there has finished
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) {
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
     mbar_init(sm.kv_full(), 1);
+    mbar_init(sm.kv_free(), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(sm.q_full(s), 1);
       mbar_init(sm.do_full(s), 1);
@@ -297,14 +278,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(sm.p_full(), 256);
     mbar_init(sm.dp_full(), 1);
     mbar_init(sm.ds_full(), 256);
-    mbar_init(sm.dq_full(), 1);
-    mbar_init(sm.dq_empty(), 256);
-    mbar_init(sm.red_ready(0), 128);
-    mbar_init(sm.red_ready(1), 128);
     mbar_init(sm.dkv_done(), 1);
     mbar_init(sm.drain(), 1);
-    mbar_init(sm.q_issued(), 1);
-    mbar_init(sm.kv_free(), 1);
     *abort_flag = 0;
     *issued_q = 0;
     *issued_do = 0;
@@ -316,7 +291,6 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_dq);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::TM_COLS);
@@ -335,9 +309,9 @@ __global__ void __launch_bounds__(384, 1)
     const int n_items = wl_count(sc);
     // ------------------------------------------------------------ producer --
     // Per item: K and V (once the previous item's last products reading them
-    // have run), then Q_t + nl_t + nd_t and dO_t of every query tile through the
-    // ring.  T counts query tiles over all of the CTA's items (ring slot and
-    // barrier phases).
+    // have been issued and run), then Q_t + nl_t + nd_t and dO_t of every query
+    // tile through the ring.  T counts query tiles over all of the CTA's items
+    // (ring slot and barrier phases).
     if (lane == 0) {
       int T = 0, ni = 0;
       bool go = true;
@@ -373,7 +347,6 @@ __global__ void __launch_bounds__(384, 1)
           bulk_load(sbase + L::OFF_STAT + st * 1024, p.nl + ws, 512, sm.q_full(st));
           bulk_load(sbase + L::OFF_STAT + st * 1024 + 512, p.nd + ws, 512, sm.q_full(st));
           *issued_q = T + 1;
-          mbar_arrive(sm.q_issued());
           if (T >= STAGES && !mbar_wait(sm.do_empty(st), eph, wc, ST_BWD_TIMEOUT_EMPTY)) {
             go = false;
             break;
@@ -409,30 +382,29 @@ __global__ void __launch_bounds__(384, 1)
     // the whole warp runs the issue code; lane 0 issues (see umma_ss_w)
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, L::BM, false, false);  // K Q^T, V dO^T
     constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, true, false);       // P^T dO, dS^T Q
-    constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, L::BM, true, true);      // K^T dS
     // Descriptors of the operand bases; an operand at byte offset `off` from a
     // base is that descriptor plus off >> 4 (the start-address field is the
     // low 14 bits and every shared address here is below 2^18, so no carry).
-    const uint64_t d_k = sdesc_sw128(sbase + L::OFF_K, 16, 1024);        // K-major: K, V, Q, dO
+    const uint64_t d_k = sdesc_sw128(sbase + L::OFF_K, 16, 1024);  // K-major: K, V, Q, dO
     const uint64_t d_v = sdesc_sw128(sbase + L::OFF_V, 16, 1024);
     const uint64_t d_q = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
     const uint64_t d_do = sdesc_sw128(sbase + L::OFF_DO, 16, 1024);
-    const uint64_t m_k = sdesc_sw128(sbase + L::OFF_K, L::COLBLK, 1024);  // MN-major: K, Q, dO, dS
-    const uint64_t m_q = sdesc_sw128(sbase + L::OFF_Q, L::COLBLK, 1024);
+    const uint64_t m_q = sdesc_sw128(sbase + L::OFF_Q, L::COLBLK, 1024);  // MN-major: Q, dO
     const uint64_t m_do = sdesc_sw128(sbase + L::OFF_DO, L::COLBLK, 1024);
-    const uint64_t m_ds = sdesc_sw128(sbase + L::OFF_DS, L::COLBLK, 1024);
     constexpr uint32_t TILE16 = L::TILE >> 4;
 
     // S^T = K Q_t^T or dP^T = V dO_t^T: both operands K-major, two column blocks each
-    auto mma_scores = [&](uint32_t d_tm, uint64_t a, uint64_t b) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
-        umma_ss_w(d_tm, a + off, b + off, IDESC_S, kk > 0 ? 1u : 0u);
-      }
+    static_assert(D == 128 && L::COLBLK == 16384 && L::BM == 128, "group issue shapes");
+    auto mma_scores = [&](uint32_t d_tm, uint64_t a, uint64_t b) { umma_ss_k8(d_tm, a, b, IDESC_S, 0u); };
+    // dV += P^T dO_t (A = P^T) or dK += dS^T Q_t (A = dS^T): A from tensor memory,
+    // bf16 pairs with queries 0-63 in columns [0, 32) and 64-127 in [64, 96) of
+    // its region (each warpgroup's half in its own columns); B MN-major, 16
+    // queries = 2 KB per step.  The accumulator starts over at an item's first tile.
+    auto mma_grad = [&](uint32_t d_tm, uint32_t a_tm, uint64_t b, bool first) {
+      umma_ts_h_mn8(d_tm, a_tm, b, IDESC_G, first ? 0u : 1u);
     };
     // Per item: MMA1_0, MMA2_0, then per tile t
-    //   MMA3_t, MMA4_t, MMA5_t, MMA1_{t+1}, MMA2_{t+1}
+    //   MMA3_t, MMA1_{t+1}, MMA4_t, MMA2_{t+1}.
     // T0 is the CTA-wide index of the item's first query tile.
     int T0 = 0, ni = 0;
     bool ok = true;
@@ -441,65 +413,40 @@ __global__ void __launch_bounds__(384, 1)
       if (n_it == 0) continue;
       const int s0 = T0 % STAGES;
       const uint32_t ph0 = (T0 / STAGES) & 1;
+      // S columns: the previous item's last P^T was read by its MMA3, issued
+      // before; dP columns: its last dS^T by its MMA4, issued before
       ok = mbar_wait_w(sm.kv_full(), ni & 1, wc, ST_BWD_TIMEOUT_KV) &&
            mbar_wait_w(sm.q_full(s0), ph0, wc, ST_BWD_TIMEOUT_Q);
       if (!ok) break;
       tc_fence_after();
-      // S columns: the previous item's last P^T was read by its MMA3, issued before
       mma_scores(tmem + L::TM_S, d_k, d_q + s0 * TILE16);
       umma_commit_w(sm.s_full());
-      // dP columns: the previous item's last dQ^T must have been read out
-      ok = (T0 == 0 || mbar_wait_w(sm.dq_empty(), (T0 - 1) & 1, wc, ST_BWD_TIMEOUT_DQE)) &&
-           mbar_wait_w(sm.do_full(s0), ph0, wc, ST_BWD_TIMEOUT_Q);
-      if (!ok) break;
+      if (!mbar_wait_w(sm.do_full(s0), ph0, wc, ST_BWD_TIMEOUT_Q)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       mma_scores(tmem + L::TM_DP, d_v, d_do + s0 * TILE16);
       umma_commit_w(sm.dp_full());
+      if (n_it == 1) umma_commit_w(sm.kv_free());  // no later product reads K or V
       for (int t = 0; t < n_it; ++t) {
         const int T = T0 + t;
         const int st = T % STAGES, st1 = (T + 1) % STAGES;
         const uint32_t ph = T & 1, ph1 = ((T + 1) / STAGES) & 1;
         const bool next = t + 1 < n_it;
-        // MMA3: dV += P^T_t dO_t (dV starts over at t = 0: the warpgroups
-        // arrive on p_full for an item only after writing out the previous
-        // item's dV and dK).  A = P^T from tensor memory: queries 0-63 in
-        // columns [0, 32), queries 64-127 in [64, 96) (each half in its own
-        // S columns); B = dO_t MN-major (16 queries = 2 KB per step).
+        // MMA3: dV += P^T_t dO_t (dV starts over at t = 0: the warpgroups arrive
+        // on p_full for an item only after writing out the previous item's dV and
+        // dK).  Its commit also covers MMA2_t, the other reader of dO_t.
         if (!mbar_wait_w(sm.p_full(), ph, wc, ST_BWD_TIMEOUT_P)) {
           ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < L::BM / 16; ++kk) {
-          const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + pcol, m_do + st * TILE16 + kk * (2048 >> 4), IDESC_G,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!mbar_wait_w(sm.ds_full(), ph, wc, ST_BWD_TIMEOUT_DS)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // MMA4: dK += dS^T_t Q_t.  A = dS^T (bf16) from the dP columns, laid out
-        // like P^T; B = Q_t MN-major.
-#pragma unroll
-        for (int kk = 0; kk < L::BM / 16; ++kk) {
-          const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_ts_w(tmem + L::TM_DK, tmem + L::TM_DP + pcol, m_q + st * TILE16 + kk * (2048 >> 4), IDESC_G,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        // MMA5: dQ^T_t = K^T dS_t into the dP columns, after MMA4 has read dS^T
-        // there.  A = K MN-major, B = dS^T read as [query][key] MN-major (two
-        // 64-query blocks, 16 KB apart).
-#pragma unroll
-        for (int kk = 0; kk < L::BN / 16; ++kk)
-          umma_ss_w(tmem + L::TM_DP, m_k + kk * (2048 >> 4), m_ds + kk * (2048 >> 4), IDESC_Q, kk > 0 ? 1u : 0u);
-        // also MMA1_t .. MMA4_t: Q_t's and dO_t's buffers are free for the dQ staging
-        umma_commit_w(sm.dq_full());
+        mma_grad(tmem + L::TM_DV, tmem + L::TM_S, m_do + st * TILE16, t == 0);
+        umma_commit_w(sm.do_empty(st));
+        // MMA1: S^T_{t+1} into the S columns (P^T_t was read by MMA3_t, issued
+        // before: the tensor cores run in issue order)
         if (next) {
-          // MMA1: S^T_{t+1} into the S columns (P^T_t was read by MMA3_t, issued
-          // before: the tensor cores run in issue order).
           if (!mbar_wait_w(sm.q_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) {
             ok = false;
             break;
@@ -507,21 +454,29 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           mma_scores(tmem + L::TM_S, d_k, d_q + st1 * TILE16);
           umma_commit_w(sm.s_full());
-          // MMA2: dP^T_{t+1} into the dP columns once dQ^T_t has been read out.
-          // Its commit also covers MMA5_t, the last reader of the dS buffer.
-          if (!mbar_wait_w(sm.dq_empty(), ph, wc, ST_BWD_TIMEOUT_DQE) ||
-              !mbar_wait_w(sm.do_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) {
+        }
+        // MMA4: dK += dS^T_t Q_t; its commit frees Q_t's stage (MMA1_t read it before)
+        if (!mbar_wait_w(sm.ds_full(), ph, wc, ST_BWD_TIMEOUT_DS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_grad(tmem + L::TM_DK, tmem + L::TM_DP, m_q + st * TILE16, t == 0);
+        umma_commit_w(sm.q_empty(st));
+        // MMA2: dP^T_{t+1} into the dP columns (dS^T_t was read by MMA4_t)
+        if (next) {
+          if (!mbar_wait_w(sm.do_full(st1), ph1, wc, ST_BWD_TIMEOUT_Q)) {
             ok = false;
             break;
           }
           tc_fence_after();
           mma_scores(tmem + L::TM_DP, d_v, d_do + st1 * TILE16);
           umma_commit_w(sm.dp_full());
+          if (t + 2 == n_it) umma_commit_w(sm.kv_free());  // the item's last reader of K and V
         }
       }
       if (!ok) break;
       umma_commit_w(sm.dkv_done());  // dV, dK of the item are complete
-      umma_commit_w(sm.kv_free());   // K and V are no longer read
       T0 += n_it;
       ++ni;
     }
@@ -532,55 +487,6 @@ __global__ void __launch_bounds__(384, 1)
     cta_bar_sync<384>();
     tc_fence_after();
     tmem_dealloc(tmem, L::TM_COLS);
-  } else if (warp == 2) {
-    reg_lower<BWD_REGS_LOW>();
-    const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
-    const uint32_t sbase = sm.base;
-    const WaitCtl wc{abort_flag, p.status, p.timeout_ns};
-    const int n_items = wl_count(sc);
-    // ----------------------------------------------------- dQ reduce-adds --
-    // Per tile: the half staged in Q_t's buffer (queries 64-127) first, then the
-    // half in dO_t's buffer (0-63); each buffer goes back to the producer once
-    // its reduce-add has read it.  Q_{t+2} is needed sooner than dO_{t+2} (its
-    // S^T product comes first), and the SM's TMA unit serves its requests in
-    // order, so within an item the load of Q_{t+2} is let in between the two
-    // reduce-adds: the second one is issued only after the producer has issued
-    // that load.  A reduce-add reads its 32 KB at about 20-25 bytes per cycle
-    // (the SM's rate for reductions into global memory), so the two take about
-    // as long as the tile's products.
-    if (lane == 0) {
-      int T0 = 0;
-      bool go = true;
-      for (int k = 0; go && k < n_items; ++k) {
-        const BwdItem g = bwd_item<L::BN, L::BM>(p, sc, k);
-        for (int t = 0; t < g.n_it; ++t) {
-          const int T = T0 + t;
-          const int st = T % STAGES;
-          const int q0 = (g.i0 + t) * L::BM;
-          if (!mbar_wait(sm.red_ready(1), T & 1, wc, ST_BWD_TIMEOUT_RED)) {
-            go = false;
-            break;
-          }
-          tma_reduce_add_3d(&tm_dq, sbase + L::OFF_Q + st * L::TILE, 0, q0 + 64, g.bh);
-          bulk_commit_group();
-          bulk_wait_read<0>();
-          mbar_arrive(sm.q_empty(st));
-          if ((t + STAGES < g.n_it && !mbar_wait(sm.q_issued(), (T + STAGES) & 1, wc, ST_BWD_TIMEOUT_RED)) ||
-              !mbar_wait(sm.red_ready(0), T & 1, wc, ST_BWD_TIMEOUT_RED)) {
-            go = false;
-            break;
-          }
-          tma_reduce_add_3d(&tm_dq, sbase + L::OFF_DO + st * L::TILE, 0, q0, g.bh);
-          bulk_commit_group();
-          bulk_wait_read<0>();
-          mbar_arrive(sm.do_empty(st));
-        }
-        T0 += g.n_it;
-      }
-      // the CTA may not exit while a reduce-add still reads its shared memory
-      bulk_wait_all();
-    }
-    cta_bar_sync<384>();
   } else if (warp >= 4) {
     reg_raise<BWD_REGS_HIGH>();
     const BwdSmem<STAGES> sm(smem_u32_fresh(smem_raw));
@@ -590,15 +496,13 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     // ---------------------------------------------------- elementwise WGs --
     // Both warpgroups take every tile: warpgroup h owns query columns
-    // [64 h, 64 h + 64).  Thread r is key row r (TMEM lane r) of S^T and dP^T,
-    // and head-dim column r (TMEM lane r) of dQ^T.
+    // [64 h, 64 h + 64).  Thread r is key row r (TMEM lane r) of S^T and dP^T.
     const int h = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + L::TM_S + h * 64;   // this half's S^T, then its P^T
-    const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T, then dQ^T
+    const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T, then its dS^T
     const float sl = p.scale_log2, scale = p.scale;
-    const uint32_t ds_row = sbase + L::OFF_DS + h * L::COLBLK + r * 128;
     const uint32_t stat = sbase + L::OFF_STAT + h * 256;  // + stage * 1024: nl; + 512: nd
     bool ok = true;
     int T0 = 0, ni = 0;
@@ -607,148 +511,104 @@ __global__ void __launch_bounds__(384, 1)
       const int bh = g.bh, k0 = g.k0, i0 = g.i0, n_it = g.n_it;
       const bool key_ok = (k0 + r) < g.kv_limit;
       const int jrow = k0 + r - p.qoff + 1;  // causal: first visible query row of key k0 + r
-      // Pass t drains dQ^T_t, then forms P^T and dS^T of tile u = t + 1:
-      //   dQ^T_t -> staged row-major for its reduce-add  |  P^T_u  |  dS^T_u
-      // (dS^T_u waits for dP^T_u, which MMA2_u writes only after the drain, so
-      // P^T_u fits in that wait either way; this order keeps P^T_u's registers
-      // out of the drain.)  T = T0 + t counts query tiles over the CTA's items.
-      for (int t = n_it > 0 ? -1 : 0; t < n_it; ++t) {
-        float pr[64];  // P^T_u of this thread's key row, from the second part to the last
-        const int u = t + 1;
-        const int T = T0 + t, U = T0 + u;
-        const int su = U % STAGES;
-        const int qu = (i0 + u) * L::BM + h * 64;  // first query of this half of tile u
-        if (t >= 0) {
-          // dQ^T_t: lane r holds head-dim column r of this half's 64 query rows.
-          // Stage them row-major -- warpgroup 0 in dO_t's buffer, warpgroup 1 in
-          // Q_t's buffer, both free since every reader of Q_t and dO_t ran before
-          // MMA5_t -- for one tiled reduce-add into global dQ each (rows past N are
-          // skipped by the tensor map).  A warp's 32 lanes write 128 consecutive
-          // bytes per store; after the second load the dP columns are free for
-          // MMA2_{t+1}.
-          if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), T & 1, wc, ST_BWD_TIMEOUT_DQ))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t out_row = sbase + (h == 0 ? L::OFF_DO : L::OFF_Q) + (T % STAGES) * L::TILE + r * 4;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t qr[32];
-            FA_TMEM_LD32(dp_col + half * 32, qr);
-            tmem_wait_ld();
-            FA_REG_FENCE32(qr);
-            if (half == 1) {
-              tc_fence_before();
-              mbar_arrive(sm.dq_empty());
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) st_shared_f32(out_row + (half * 32 + j) * 512, __uint_as_float(qr[j]));
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(sm.red_ready(h));
+      for (int t = 0; t < n_it; ++t) {
+        const int T = T0 + t;
+        const int st = T % STAGES;
+        const int q0 = (i0 + t) * L::BM + h * 64;  // first query of this half of tile t
+        // q_full is already complete here (S^T_t exists); waiting on it makes the
+        // stage's nl / nd rows visible to these threads
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.s_full(), T & 1, wc, ST_BWD_TIMEOUT_S) &&
+                                         mbar_wait(sm.q_full(st), (T / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
+          ok = false;
+          break;
         }
-
-        if (u < n_it) {
-          // q_full is already complete here (S^T_u exists); waiting on it makes the
-          // stage's nl / nd rows visible to these threads
-          if (!__all_sync(0xffffffffu, mbar_wait(sm.s_full(), U & 1, wc, ST_BWD_TIMEOUT_S) &&
-                                           mbar_wait(sm.q_full(su), (U / STAGES) & 1, wc, ST_BWD_TIMEOUT_Q))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // causal: key k0 + r is visible to query qu + j iff k0 + r < qu + j + qoff
-          const int jmin = p.causal ? jrow - qu : -1;
+        tc_fence_after();
+        float pr[64];  // P^T_t of this thread's key row over the half's 64 queries
+        {
+          uint32_t sr[64];
+          FA_TMEM_LD32(s_col, sr);
+          FA_TMEM_LD32(s_col + 32, sr + 32);
+          tmem_wait_ld();
+          FA_REG_FENCE32(sr);
+          FA_REG_FENCE32(sr + 32);
+          // causal: key k0 + r is visible to query q0 + j iff k0 + r < q0 + j + qoff
+          const int jmin = p.causal ? jrow - q0 : -1;
           // only tiles on the diagonal or past a key-padding edge mask anything
-          const bool masked = __any_sync(0xffffffffu, !key_ok || jmin > 0);
-          const uint32_t nl_s = stat + su * 1024;
+          if (__any_sync(0xffffffffu, !key_ok || jmin > 0)) {
+#pragma unroll
+            for (int w = 0; w < 64; ++w)
+              if (!key_ok || w < jmin) sr[w] = __float_as_uint(-INFINITY);
+          }
+          const uint32_t nl_s = stat + st * 1024;
           const uint64_t sl2 = f2_pack(sl, sl);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t sr[32];
-            FA_TMEM_LD32(s_col + half * 32, sr);
-            tmem_wait_ld();
-            FA_REG_FENCE32(sr);
-            if (masked) {
+          for (int j4 = 0; j4 < 64; j4 += 4) {
+            float nl[4];
+            ld_shared_v4f(nl_s + j4 * 4, nl);
 #pragma unroll
-              for (int w = 0; w < 32; ++w)
-                if (!key_ok || half * 32 + w < jmin) sr[w] = __float_as_uint(-INFINITY);
-            }
-#pragma unroll
-            for (int j4 = 0; j4 < 32; j4 += 4) {
-              float nl[4];
-              ld_shared_v4f(nl_s + (half * 32 + j4) * 4, nl);
-#pragma unroll
-              for (int w = 0; w < 4; w += 2) {
-                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
-                                           f2_pack(nl[w], nl[w + 1]));
-                constexpr int E = FA_BWD_EXP2_FMA_EVERY > 0 ? FA_BWD_EXP2_FMA_EVERY : 1;
-                if (FA_BWD_EXP2_FMA_EVERY > 0 && ((j4 + w) / 2 + 1) % E == 0) {
-                  f2_unpack(exp2_fma2(x2), pr[half * 32 + j4 + w], pr[half * 32 + j4 + w + 1]);  // FMA pipe
-                } else {
-                  float x0, x1;
-                  f2_unpack(x2, x0, x1);
-                  pr[half * 32 + j4 + w] = ex2_approx(x0);
-                  pr[half * 32 + j4 + w + 1] = ex2_approx(x1);
-                }
+            for (int w = 0; w < 4; w += 2) {
+              const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[j4 + w]), __uint_as_float(sr[j4 + w + 1])), sl2,
+                                         f2_pack(nl[w], nl[w + 1]));
+              constexpr int E = FA_BWD_EXP2_FMA_EVERY > 0 ? FA_BWD_EXP2_FMA_EVERY : 1;
+              if (FA_BWD_EXP2_FMA_EVERY > 0 && ((j4 + w) / 2 + 1) % E == 0) {
+                f2_unpack(exp2_fma2(x2), pr[j4 + w], pr[j4 + w + 1]);  // FMA pipe
+              } else {
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                pr[j4 + w] = ex2_approx(x0);
+                pr[j4 + w + 1] = ex2_approx(x1);
               }
             }
           }
+        }
+        {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
           FA_TMEM_ST32(s_col, pk);
           tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(sm.p_full());
+        }
+        tc_fence_before();
+        mbar_arrive(sm.p_full());
 
-          // dP^T_u; its commit also covers MMA5_t, so the dS buffer is free
-          if (!__all_sync(0xffffffffu, mbar_wait(sm.dp_full(), U & 1, wc, ST_BWD_TIMEOUT_DP))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t nd_s = stat + su * 1024 + 512;
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.dp_full(), T & 1, wc, ST_BWD_TIMEOUT_DP))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          uint32_t dpr[64];
+          FA_TMEM_LD32(dp_col, dpr);
+          FA_TMEM_LD32(dp_col + 32, dpr + 32);
+          tmem_wait_ld();
+          FA_REG_FENCE32(dpr);
+          FA_REG_FENCE32(dpr + 32);
+          const uint32_t nd_s = stat + st * 1024 + 512;
           const uint64_t sc2 = f2_pack(scale, scale);
           uint32_t dsk[32];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t dpr[32];
-            FA_TMEM_LD32(dp_col + half * 32, dpr);
-            tmem_wait_ld();
-            FA_REG_FENCE32(dpr);
+          for (int j4 = 0; j4 < 64; j4 += 4) {
+            float nd[4];
+            ld_shared_v4f(nd_s + j4 * 4, nd);
 #pragma unroll
-            for (int j4 = 0; j4 < 32; j4 += 4) {
-              const int j = half * 32 + j4;
-              float nd[4];
-              ld_shared_v4f(nd_s + j * 4, nd);
-#pragma unroll
-              for (int w = 0; w < 4; w += 2) {
-                // dS = P (dP scale - D scale)
-                const uint64_t g =
-                    f2_mul(f2_fma(f2_pack(__uint_as_float(dpr[j4 + w]), __uint_as_float(dpr[j4 + w + 1])), sc2,
-                                  f2_pack(nd[w], nd[w + 1])),
-                           f2_pack(pr[j + w], pr[j + w + 1]));
-                float g0, g1;
-                f2_unpack(g, g0, g1);
-                dsk[(j + w) / 2] = pack_bf16x2(g0, g1);
-              }
+            for (int w = 0; w < 4; w += 2) {
+              // dS = P (dP scale - D scale)
+              const uint64_t gr =
+                  f2_mul(f2_fma(f2_pack(__uint_as_float(dpr[j4 + w]), __uint_as_float(dpr[j4 + w + 1])), sc2,
+                                f2_pack(nd[w], nd[w + 1])),
+                         f2_pack(pr[j4 + w], pr[j4 + w + 1]));
+              float g0, g1;
+              f2_unpack(gr, g0, g1);
+              dsk[(j4 + w) / 2] = pack_bf16x2(g0, g1);
             }
           }
           // dS^T as MMA4's A operand: bf16 pairs into the first 32 of this half's
-          // dP columns (dP^T has been read into registers) ...
+          // dP columns (dP^T has been read into registers)
           FA_TMEM_ST32(dp_col, dsk);
-          // ... and as MMA5's B operand: row r of this half's 128B-swizzled block,
-          // 16-byte chunk c at c ^ (r & 7).
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
           tmem_wait_st();
-          tc_fence_before();
-          fence_proxy_async_smem();
-          mbar_arrive(sm.ds_full());
         }
+        tc_fence_before();
+        mbar_arrive(sm.ds_full());
       }
 
       // ---------------------------------------------------------- epilogue --
@@ -791,7 +651,7 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_before();
     cta_bar_sync<384>();
   } else {
-    reg_lower<BWD_REGS_LOW>();  // warp 3: no role
+    reg_lower<BWD_REGS_LOW>();  // warps 2-3: no role
     cta_bar_sync<384>();
   }
 }

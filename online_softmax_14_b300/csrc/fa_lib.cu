@@ -24,6 +24,7 @@
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
 #include "bwd_tc.cuh"
+#include "bwd_dq.cuh"
 #include "merge.cuh"
 #include "std_attn.cuh"
 
@@ -146,9 +147,12 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaFuncSetAttribute(fa::fwd_bf16_tc_kernel<64, kSlotsD64>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, L64::BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
-    if ((e = cudaFuncSetAttribute(fa::bwd_bf16_tc_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(fa::bwd_dkdv_kernel<kStagesBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fa::BwdLayout<kStagesBwd>::BYTES)) != cudaSuccess)
-      return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+      return cuda_fail(e, "cudaFuncSetAttribute(bwd dK dV)");
+    if ((e = cudaFuncSetAttribute(fa::bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  fa::DqLayout::BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(bwd dQ)");
     if ((e = cudaFuncSetAttribute(fa::std_gemm_kernel<kStagesStdS, false, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fa::StdGemmLayout<kStagesStdS>::BYTES)) != cudaSuccess)
@@ -207,22 +211,6 @@ fa_status make_map_strided(CUtensorMap* m, const void* base, int cols, int rows,
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
-  return FA_OK;
-}
-
-// [BH, N, d] f32 viewed as a 3-D tensor (d innermost); d x rows x 1 boxes, no
-// swizzle (a box is `rows` consecutive rows of d floats).  Used as the target of
-// tiled reduce-adds, which skip the rows past N.
-fa_status make_map_f32(CUtensorMap* m, void* base, int d, int N, int BH, const char* name, int rows) {
-  auto enc = encode_fn();
-  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
   return FA_OK;
 }
@@ -330,6 +318,7 @@ const fa::WorkList* fwd_work_list(int BH, int N, int Nk, int causal, int qoff, i
   return work_list(WorkKey{0, BH, N, Nk, causal, qoff, D, G}, w, 2.0 * Nk * D * 2);  // K and V of a head
 }
 
+// dK/dV kernel: units are the key tiles of a head
 const fa::WorkList* bwd_work_list(int BH, int N, int Nk, int causal, int qoff, int D, int G) {
   const int n_qt = (N + 127) / 128, n_kt = (Nk + 127) / 128;
   std::vector<int> w(n_kt);
@@ -340,6 +329,14 @@ const fa::WorkList* bwd_work_list(int BH, int N, int Nk, int causal, int qoff, i
   }
   // Q, dO, K and V of a head
   return work_list(WorkKey{1, BH, N, Nk, causal, qoff, D, G}, w, 2.0 * (N + Nk) * D * 2);
+}
+
+// dQ kernel: units are the query tiles of a head
+const fa::WorkList* dq_work_list(int BH, int N, int Nk, int causal, int qoff, int D, int G) {
+  const int n_qt = (N + 127) / 128;
+  std::vector<int> w(n_qt);
+  for (int qt = 0; qt < n_qt; ++qt) w[qt] = tiles_needed(qt, n_qt, N, Nk, causal, qoff) + 2;
+  return work_list(WorkKey{3, BH, N, Nk, causal, qoff, D, G}, w, 2.0 * (N + Nk) * D * 2);
 }
 
 template <int D, int STAGES>
@@ -404,27 +401,27 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   const int BH = B * H;
   const long long Np = bwd_np(N);
   const long long pre_blocks = static_cast<long long>(BH) * (Np / 64);
-  const long long n_kt = (Nk + L::BN - 1) / L::BN;
-  const long long n_items = n_kt * BH;
-  if (pre_blocks > 0x7fffffffll || n_items > 0x7fffffffll) return fail(FA_ERR_UNSUPPORTED, "grid too large");
-  // persistent grid: one CTA per SM, fewer when there are fewer key tiles
-  const int G = static_cast<int>(std::min<long long>(std::max(1, ds.sm_count), n_items));
+  const long long n_kt = (Nk + L::BN - 1) / L::BN, n_qt = (N + fa::DqLayout::BM - 1) / fa::DqLayout::BM;
+  const long long kv_items = n_kt * BH, q_items = n_qt * BH;
+  if (pre_blocks > 0x7fffffffll || kv_items > 0x7fffffffll || q_items > 0x7fffffffll)
+    return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  // persistent grids: one CTA per SM, fewer when there are fewer tiles
+  const int G_kv = static_cast<int>(std::min<long long>(std::max(1, ds.sm_count), kv_items));
+  const int G_q = static_cast<int>(std::min<long long>(std::max(1, ds.sm_count), q_items));
 
   // every tensor map is built before anything is enqueued, so that a failure
   // here leaves the stream untouched
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo;
   fa_status s;
   if ((s = make_map(&mq, q, D, N, BH, "q", 128)) != FA_OK) return s;
   if ((s = make_map(&mk, k, D, Nk, BH, "k", 128)) != FA_OK) return s;
   if ((s = make_map(&mv, v, D, Nk, BH, "v", 128)) != FA_OK) return s;
   if ((s = make_map(&mdo, dO, D, N, BH, "dO", 128)) != FA_OK) return s;
-  if ((s = make_map_f32(&mdq, dq, D, N, BH, "dq", 64)) != FA_OK) return s;
 
   fa::BwdPreParams pp{};
   pp.o = static_cast<const __nv_bfloat16*>(o);
   pp.dO = static_cast<const __nv_bfloat16*>(dO);
   pp.lse = lse;
-  pp.dq = dq;
   pp.nl = ws;
   pp.nd = ws + static_cast<size_t>(BH) * Np;
   pp.BH = BH;
@@ -441,12 +438,14 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.dv = dv;
   p.nl = pp.nl;
   p.nd = pp.nd;
+  p.q = static_cast<const __nv_bfloat16*>(q);
   p.kv_len = kv_len;
   p.BH = BH;
   p.H = H;
   p.N = N;
   p.Np = static_cast<int>(Np);
   p.Nk = Nk;
+  p.n_qt = static_cast<int>(n_qt);
   p.n_kt = static_cast<int>(n_kt);
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -455,10 +454,25 @@ fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
   p.status = ds.status;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.load();
-  const fa::WorkList* wl = bwd_work_list(BH, N, Nk, causal, p.qoff, D, G);
-  fa::bwd_bf16_tc_kernel<kStagesBwd>
-      <<<static_cast<unsigned>(G), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, mdq, p, *wl);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_bf16_tc_kernel");
+  const fa::WorkList* wl_kv = bwd_work_list(BH, N, Nk, causal, p.qoff, D, G_kv);
+  fa::bwd_dkdv_kernel<kStagesBwd><<<static_cast<unsigned>(G_kv), 384, L::BYTES, stream>>>(mq, mk, mv, mdo, p, *wl_kv);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch bwd_dkdv_kernel");
+  const fa::WorkList* wl_q = dq_work_list(BH, N, Nk, causal, p.qoff, D, G_q);
+  // programmatic stream serialization: the dQ kernel's CTAs start on the SMs the
+  // dK/dV kernel's CTAs leave (it reads nothing that kernel writes, and waits for
+  // it before completing)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(G_q));
+  cfg.blockDim = dim3(384);
+  cfg.dynamicSmemBytes = fa::DqLayout::BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, fa::bwd_dq_kernel, mk, mv, mdo, p, *wl_q)) != cudaSuccess)
+    return cuda_fail(e, "launch bwd_dq_kernel");
   return FA_OK;
 }
 

@@ -129,6 +129,17 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return mbar_wait_drain(smem_u32(bar), parity, limit_ns);
 }
 
+// ---------------------------------------------- programmatic dependent launch ---
+// Lets the next kernel on the stream, launched with programmatic stream
+// serialization, start its CTAs once every CTA of this grid has executed this
+// (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one was allowed to overlap have completed and their
+// memory operations are visible (returns at once without such a dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // -------------------------------------------------------------------- TMA ---
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -156,44 +167,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (the tensor cores read MMA operands through it).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-// 3-D tiled reduce-add shared -> global (element-wise atomic add of the box at
-// the given coordinates), tracked by this thread's bulk async-group.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(src), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until at most N of this thread's committed bulk groups are still reading their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Wait until every committed bulk operation of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 __device__ __forceinline__ void ld_shared_v4f(uint32_t addr, float* v) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
                : "r"(addr)
                : "memory");
 }
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05 ---
 // Tensor-memory allocation (whole warp).  The allocated base address is written
 // to shared memory at `dst`.
@@ -216,10 +195,9 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // tcgen05.mma, issued from a converged warp: D[tmem] (+)= A * B, bf16 in, f32
-// accumulate; A from shared memory (umma_ss_w) or tensor memory (umma_ts_w), B
-// from shared memory.  All 32 lanes of the issuing warp run the issue code (the
-// operands are warp-uniform) and lane 0 alone executes the tensor-core
-// instruction through a predicate.  Measured on B300: a barrier test between two
+// accumulate, A and B from shared memory.  All 32 lanes of the issuing warp run
+// the issue code (the operands are warp-uniform) and lane 0 alone executes the
+// tensor-core instruction through a predicate.  Measured on B300: a barrier test between two
 // groups of MMAs stalls the tensor pipe for ~190 cycles when one lane runs the
 // issue code on its own, and for ~20 cycles when the warp stays converged.
 __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -232,16 +210,64 @@ __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
-      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// A whole K = 16 NK group of MMAs in one asm block: lane 0 of the converged warp
+// issues NK tcgen05.mma, the first accumulating iff `accumulate` != 0 and the
+// rest always accumulating.  Operand addresses of step kk are the base plus a
+// fixed offset: descriptor offsets in 16-byte units (the start-address field),
+// tensor-memory A offsets in columns.  Measured on B300: a group of 8 goes out in
+// about 15 cycles this way, against about 300 when each MMA is its own asm
+// statement, and the issuing warp is free again that much sooner.
+//   *_k8 / *_k4: K-major shared-memory operand, 128-byte swizzle, two 16 KB
+//                column blocks of 64 elements (steps 0-3 in the first, 4-7 in the
+//                second), 32 bytes per step;
+//   *_mn8:       MN-major shared-memory B, 16 rows (2 KB) per step;
+//   A in tensor memory (ts): 8 columns per step, contiguous (_c) or split in
+//                two 32-column halves 64 columns apart (_h).
+#define FA_UMMA_HEAD                                                                               \
+  "{\n\t.reg .pred e, p;\n\t.reg .b32 l, t1;\n\t.reg .b64 a1, b1;\n\t"                             \
+  "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+#define FA_UMMA_SS_FIRST "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+#define FA_UMMA_TS_FIRST "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+#define FA_UMMA_SS(OA, OB)                                                                         \
+  "add.s64 a1, %1, " #OA ";\n\tadd.s64 b1, %2, " #OB ";\n\t"                                       \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+#define FA_UMMA_TS(OA, OB)                                                                         \
+  "add.u32 t1, %1, " #OA ";\n\tadd.s64 b1, %2, " #OB ";\n\t"                                       \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], b1, %3, 1;\n\t"
+
+__device__ __forceinline__ void umma_ss_k8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_UMMA_HEAD FA_UMMA_SS_FIRST FA_UMMA_SS(2, 2) FA_UMMA_SS(4, 4) FA_UMMA_SS(6, 6)
+                   FA_UMMA_SS(1024, 1024) FA_UMMA_SS(1026, 1026) FA_UMMA_SS(1028, 1028) FA_UMMA_SS(1030, 1030) "}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+               : "memory");
 }
+__device__ __forceinline__ void umma_ss_k4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_UMMA_HEAD FA_UMMA_SS_FIRST FA_UMMA_SS(2, 2) FA_UMMA_SS(4, 4) FA_UMMA_SS(6, 6) "}" ::"r"(d), "l"(a),
+               "l"(b), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+// A from tensor memory (contiguous), B MN-major
+__device__ __forceinline__ void umma_ts_c_mn8(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_UMMA_HEAD FA_UMMA_TS_FIRST FA_UMMA_TS(8, 128) FA_UMMA_TS(16, 256) FA_UMMA_TS(24, 384)
+                   FA_UMMA_TS(32, 512) FA_UMMA_TS(40, 640) FA_UMMA_TS(48, 768) FA_UMMA_TS(56, 896) "}" ::"r"(d),
+               "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+// A from tensor memory (two halves 64 columns apart), B MN-major
+__device__ __forceinline__ void umma_ts_h_mn8(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_UMMA_HEAD FA_UMMA_TS_FIRST FA_UMMA_TS(8, 128) FA_UMMA_TS(16, 256) FA_UMMA_TS(24, 384)
+                   FA_UMMA_TS(64, 512) FA_UMMA_TS(72, 640) FA_UMMA_TS(80, 768) FA_UMMA_TS(88, 896) "}" ::"r"(d),
+               "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+// A from tensor memory (contiguous), B K-major
+__device__ __forceinline__ void umma_ts_c_k8(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_UMMA_HEAD FA_UMMA_TS_FIRST FA_UMMA_TS(8, 2) FA_UMMA_TS(16, 4) FA_UMMA_TS(24, 6)
+                   FA_UMMA_TS(32, 1024) FA_UMMA_TS(40, 1026) FA_UMMA_TS(48, 1028) FA_UMMA_TS(56, 1030) "}" ::"r"(d),
+               "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+
 // Lane 0 (the lane that issued the MMAs) arrives once on `bar` when every
 // tcgen05.mma it has issued so far is done.
 __device__ __forceinline__ void umma_commit_w(uint32_t bar) {

@@ -135,13 +135,33 @@ def test_bwd_full_size_workload_eight_heads():
 
 
 def test_bwd_repeatable():
-    """Two calls on the same inputs agree (dQ is accumulated with atomics, so only
-    the summation order may differ)."""
-    pr = make_problem(1, 2, 256, 128, "bf16", seed=14, backward=True)
+    """Two calls on the same inputs agree bit for bit: every gradient row is
+    summed in tensor memory in a fixed order and written once, so the result
+    does not depend on the order in which CTAs run."""
+    pr = make_problem(2, 4, 1000, 128, "bf16", seed=14, backward=True)
     a = run_fwd_bwd(pr, causal=True)
     b = run_fwd_bwd(pr, causal=True)
     for x, y in zip(a, b):
-        assert np.abs(x - y).max() <= 1e-5
+        assert np.array_equal(x, y)
+
+
+def test_bwd_full_size_repeatable():
+    """At the full workload size (B=4 H=16 N=4096 d=128, causal) ten calls agree
+    bit for bit.  A hand-off between the warpgroups that let one of them run a
+    tile ahead of the other corrupted a few dQ rows in about a third of the calls
+    at this size, and in none at the small sizes above."""
+    w = WORKLOADS["bf16_causal_fwdbwd_B4_H16_N4096_d128"]
+    pr = make_workload(w)
+    m = fa()
+    q, k, v, do = (pr[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = m.attention_fwd(q, k, v, pr["scale"], causal=True)
+    first = m.attention_bwd(q, k, v, o, lse, do, pr["scale"], causal=True)
+    assert all(bool(torch.isfinite(t).all()) for t in first)
+    for _ in range(9):
+        again = m.attention_bwd(q, k, v, o, lse, do, pr["scale"], causal=True)
+        for a, b in zip(again, first):
+            assert torch.equal(a, b)
+    m.fa_check_device_error()
 
 
 @pytest.mark.parametrize("N", [64, 200, 384])
@@ -153,18 +173,20 @@ def test_bwd_strictly_causal(N):
     assert np.all(dk[:, :, N - 1] == 0) and np.all(dv[:, :, N - 1] == 0)
 
 
-def test_bwd_starved_pipeline_times_out_and_recovers():
-    """The test hook makes the backward producer stop after its first Q / dO
-    tile: every bounded wait downstream gives up, the launch reports
-    FA_ERR_TIMEOUT (the CTA drains its copies and products and frees its tensor
-    memory), and the next normal call is correct again."""
+@pytest.mark.parametrize("code", [2, 3], ids=["dkdv_producer", "dq_producer"])
+def test_bwd_starved_pipeline_times_out_and_recovers(code):
+    """The test hook makes one backward producer stop early -- code 2: the
+    dK/dV kernel's after its first Q / dO tile; code 3: the dQ kernel's after
+    its first K / V tile.  Every bounded wait downstream gives up, the launch
+    reports FA_ERR_TIMEOUT (the CTA drains its copies and products and frees its
+    tensor memory), and the next normal call is correct again."""
     m = fa()
     pr = make_problem(1, 2, 512, 128, "bf16", seed=15, backward=True)
     q, k, v, do = (pr[n].to(DEV) for n in ("q", "k", "v", "do"))
     o, lse = m.attention_fwd(q, k, v, pr["scale"], causal=False)
     m.fa_check_device_error()
     m.fa_set_wait_timeout_ms(50)
-    m.fa_debug_inject(2)
+    m.fa_debug_inject(code)
     try:
         m.attention_bwd(q, k, v, o, lse, do, pr["scale"], causal=False)
         with pytest.raises(m.FaError) as ei:
