@@ -50,17 +50,25 @@
 #include "ptx.cuh"
 #include "worklist.cuh"
 
-// Every FA_FWD_EXP2_FMA_EVERY-th pair of scores takes its exponentials on the FMA
-// pipe (exp2_fma2) instead of the special-function unit; 0 = none.
-#ifndef FA_FWD_EXP2_FMA_EVERY
-#define FA_FWD_EXP2_FMA_EVERY 0
+// Every FA_FWD_EXP2_FMA_EVERY_D<d>-th pair of scores takes its exponentials on
+// the FMA pipe (exp2_fma2) instead of the special-function unit; 0 = none.  At
+// d = 64 a key tile costs the tensor cores half as much as at d = 128 while the
+// exponentials stay the same, so there the special-function unit is the bound
+// and part of the work moves to the FMA pipe.
+#ifndef FA_FWD_EXP2_FMA_EVERY_D128
+#define FA_FWD_EXP2_FMA_EVERY_D128 0
+#endif
+#ifndef FA_FWD_EXP2_FMA_EVERY_D64
+#define FA_FWD_EXP2_FMA_EVERY_D64 0
 #endif
 
 namespace fa {
 
 // Pair i of each 16-pair quarter of a row takes the FMA-pipe exponential.
+template <int D>
 __host__ __device__ constexpr bool exp2_on_fma(int i) {
-  return FA_FWD_EXP2_FMA_EVERY > 0 && (i + 1) % (FA_FWD_EXP2_FMA_EVERY > 0 ? FA_FWD_EXP2_FMA_EVERY : 1) == 0;
+  constexpr int E = D == 64 ? FA_FWD_EXP2_FMA_EVERY_D64 : FA_FWD_EXP2_FMA_EVERY_D128;
+  return E > 0 && (i + 1) % (E > 0 ? E : 1) == 0;
 }
 
 // Register shares (launch: 384 threads x 168): warpgroup 2 (producer, MMA issuer,
@@ -484,7 +492,7 @@ __global__ void __launch_bounds__(384, 1)
             const uint64_t x2 =
                 f2_fma(f2_pack(__uint_as_float(sr[32 * h + 2 * i]), __uint_as_float(sr[32 * h + 2 * i + 1])), sl2, nm2);
             uint64_t p2;
-            if (exp2_on_fma(i)) {
+            if (exp2_on_fma<D>(i)) {
               p2 = exp2_fma2(x2);  // this pair on the FMA pipe
             } else {
               float x0, x1;
