@@ -306,11 +306,11 @@ __global__ void __launch_bounds__(384, 1)
     auto issue_s = [&](uint32_t tm_s, uint32_t q_off, uint32_t bar, int ck) {
       const uint64_t ka = dk_base + (((ck % NS) * L::TILE) >> 4);
       const uint64_t qa = dq_base + (q_off >> 4);
-      static_assert(L::COLBLK == 16384, "the group issue assumes 16 KB column blocks");
-      if constexpr (D == 128)
-        umma_ss_k8(tm_s, qa, ka, IDESC_QK, 0u);
-      else
-        umma_ss_k4(tm_s, qa, ka, IDESC_QK, 0u);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * L::COLBLK + (kk & 3) * 32) >> 4;
+        umma_ss_w(tm_s, qa + off, ka + off, IDESC_QK, kk > 0 ? 1u : 0u);
+      }
       umma_commit_w(bar);
     };
     // O_i += P_i V, V in the slot of load number cv.  Only a tile's last
@@ -319,8 +319,9 @@ __global__ void __launch_bounds__(384, 1)
     // because a commit tracks every earlier tensor-core operation of this thread.
     auto issue_pv = [&](uint32_t tm_o, uint32_t tm_p, uint32_t bar, int cv, bool first, bool last) {
       const uint64_t va = dv_base + (((cv % NS) * L::TILE) >> 4);
-      static_assert(L::BN == 128, "the group issue covers 128 keys");
-      umma_ts_c_mn8(tm_o, tm_p, va, IDESC_PV, first ? 0u : 1u);
+#pragma unroll
+      for (int kk = 0; kk < L::BN / 16; ++kk)
+        umma_ts_w(tm_o, tm_p + kk * 8, va + (kk * 2048 >> 4), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
       if (last) umma_commit_w(bar);
     };
     const uint32_t tS0 = tmem + L::TM_S0, tS1 = tmem + L::TM_S1;

@@ -195,9 +195,10 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // tcgen05.mma, issued from a converged warp: D[tmem] (+)= A * B, bf16 in, f32
-// accumulate, A and B from shared memory.  All 32 lanes of the issuing warp run
-// the issue code (the operands are warp-uniform) and lane 0 alone executes the
-// tensor-core instruction through a predicate.  Measured on B300: a barrier test between two
+// accumulate; A from shared memory (umma_ss_w) or tensor memory (umma_ts_w), B
+// from shared memory.  All 32 lanes of the issuing warp run the issue code (the
+// operands are warp-uniform) and lane 0 alone executes the tensor-core
+// instruction through a predicate.  Measured on B300: a barrier test between two
 // groups of MMAs stalls the tensor pipe for ~190 cycles when one lane runs the
 // issue code on its own, and for ~20 cycles when the warp stays converged.
 __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -208,6 +209,16 @@ __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // A whole K = 16 NK group of MMAs in one asm block: lane 0 of the converged warp
