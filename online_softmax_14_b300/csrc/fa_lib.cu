@@ -379,7 +379,7 @@ fa_status launch_tc(const void* q, const void* k, const void* v, void* o, float*
 template <int DP>
 fa_status launch_simt(const fa::SimtParams& p, cudaStream_t stream) {
   dim3 grid((p.N + fa::SIMT_ROWS - 1) / fa::SIMT_ROWS, p.BH);
-  fa::fwd_f32_simt_kernel<DP><<<grid, fa::SIMT_ROWS * 32, 0, stream>>>(p);
+  fa::fwd_f32_simt_kernel<DP><<<grid, fa::SIMT_WARPS * 32, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch fwd_f32_simt_kernel");
   return FA_OK;
