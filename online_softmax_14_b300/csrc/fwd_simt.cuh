@@ -83,11 +83,15 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) fwd_f32_simt_kernel(const Sim
     float s[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) s[r] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < DP; ++c) {
-      const float kc = (key < Nk && c < d) ? krow[c] : 0.f;
+    // the key row in chunks of 16 loads, all issued before their FMAs
+    for (int c0 = 0; c0 < DP; c0 += 16) {
+      float kc[16];
 #pragma unroll
-      for (int r = 0; r < R; ++r) s[r] = fmaf(sQ[r][c], kc, s[r]);
+      for (int i = 0; i < 16; ++i) kc[i] = (key < Nk && c0 + i < d) ? krow[c0 + i] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+#pragma unroll
+        for (int r = 0; r < R; ++r) s[r] = fmaf(sQ[r][c0 + i], kc[i], s[r]);
     }
     float pj[R];
 #pragma unroll
@@ -109,19 +113,25 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) fwd_f32_simt_kernel(const Sim
       for (int t = 0; t < CPL; ++t) acc[r][t] *= c;
       m[r] = m_new;
     }
-    // acc += p V over the block's keys; lane t owns columns lane + 32 t
-    const int nj = min(SIMT_KEYS, Nk - k0);
-    for (int j = 0; j < nj; ++j) {
-      const float* vrow = p.v + head_k + static_cast<size_t>(k0 + j) * d;
-      float vv[CPL];
+    // acc += p V over the block's keys, 8 keys at a time with their V rows loaded
+    // first; lane t owns columns lane + 32 t (keys past Nk have p = 0 and read as 0)
+    for (int j0 = 0; j0 < SIMT_KEYS; j0 += 8) {
+      float vv[8][CPL];
 #pragma unroll
-      for (int t = 0; t < CPL; ++t) vv[t] = (lane + 32 * t < d) ? vrow[lane + 32 * t] : 0.f;
+      for (int jj = 0; jj < 8; ++jj) {
+        const int kj = k0 + j0 + jj;
+        const float* vrow = p.v + head_k + static_cast<size_t>(min(kj, Nk - 1)) * d;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float pb = __shfl_sync(0xffffffffu, pj[r], j);
-#pragma unroll
-        for (int t = 0; t < CPL; ++t) acc[r][t] = fmaf(pb, vv[t], acc[r][t]);
+        for (int t = 0; t < CPL; ++t) vv[jj][t] = (kj < Nk && lane + 32 * t < d) ? vrow[lane + 32 * t] : 0.f;
       }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float pb = __shfl_sync(0xffffffffu, pj[r], j0 + jj);
+#pragma unroll
+          for (int t = 0; t < CPL; ++t) acc[r][t] = fmaf(pb, vv[jj][t], acc[r][t]);
+        }
     }
   }
 
