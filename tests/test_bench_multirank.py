@@ -85,3 +85,22 @@ def test_reference_arm_runs_on_rank0_only(tmp_path):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_forward_source_digest_covers_kernel_and_launch_only():
+    """The digest that guards the recorded DRAM traffic covers the forward's
+    headers and the host functions that shape its launch: the text of such a
+    function is extracted up to its matching brace, and a function that is not
+    there contributes nothing."""
+    import bench
+
+    src = "int a() { return 1; }\nfa_status launch_tc(int x) {\n  if (x) { return 2; }\n  return 3;\n}\nint b() {}\n"
+    assert bench._function_text(src, "fa_status launch_tc(") == (
+        "fa_status launch_tc(int x) {\n  if (x) { return 2; }\n  return 3;\n}")
+    assert bench._function_text(src, "int missing(") == ""
+    digest = bench.kernel_src_digest()
+    assert len(digest) == 16 and int(digest, 16) >= 0
+    # every host function the digest names is present in the library source
+    lib = open(os.path.join(ROOT, "online_softmax_14_b300", "csrc", "fa_lib.cu"), encoding="utf-8").read()
+    for head in bench.FWD_HOST_FUNCTIONS:
+        assert bench._function_text(lib, head).startswith(head)
