@@ -15,7 +15,7 @@
 // bwd_dq_kernel is persistent; a work item is (batch*head, 128-query tile).  Q of
 // the item sits in tensor memory (the elementwise warps write it there), dO in
 // shared memory; the key tiles K_j and V_j stream through TMA rings of three
-// slots each.  Per key tile the tensor cores run three MMAs (128 x 128 x 128):
+// and two slots.  Per key tile the tensor cores run three MMAs (128 x 128 x 128):
 //     S_j  = Q K_j^T     (A = Q from tensor memory, B = K_j K-major)
 //     dP_j = dO V_j^T    (A = dO, B = V_j, both K-major in shared memory)
 //     dQ  += dS_j K_j    (A = dS_j, bf16 in tensor memory; B = K_j MN-major)
@@ -65,11 +65,12 @@ struct DqLayout {
   static constexpr int KB = D / 64;                // 128-byte column blocks
   static constexpr int COLBLK = 128 * 128;         // 16 KB: 128 rows x 128 bytes
   static constexpr int TILE = 128 * D * 2;         // 32 KB: a dO, K or V tile
-  static constexpr int NK = 3, NV = 3;             // K and V ring slots
+  static constexpr int NK = 3, NV = 2;             // K and V ring slots
   static constexpr int OFF_DO = 0;
   static constexpr int OFF_K = TILE;
   static constexpr int OFF_V = OFF_K + NK * TILE;
-  static constexpr int OFF_BAR = OFF_V + NV * TILE;
+  static constexpr int OFF_EPI = OFF_V + NV * TILE;  // 2 KB per elementwise warp (epilogue)
+  static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
   // barriers: do_full, do_free, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready,
   //           s_full, s_free, dp_full, dp_free, ds_full, ds_free, dq_done, drain
   static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 9;
@@ -493,8 +494,10 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
       if (ok) {
         tc_fence_after();
-        float* out = p.dq + (static_cast<size_t>(g.bh) * p.N + qi) * D + h * 64;
+        const int qr0 = g.q0 + (warp & 3) * 32;  // this warp's first query row
+        const int rows = min(32, p.N - qr0);
         const uint32_t col = lane_base + L::TM_DQ + h * 64;
+        const uint32_t buf = sm.base + L::OFF_EPI + (warp - 4) * 2048;
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
           uint32_t v[32];
@@ -506,13 +509,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          if (qi < p.N) {
-            float4* o4 = reinterpret_cast<float4*>(out + cb * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          }
+          warp_store_rows_f32x32(v, buf, p.dq, static_cast<size_t>(g.bh) * p.N + qr0, D, h * 64 + cb * 32, rows);
         }
         // the next item's first dQ product overwrites dQ only after these
         // warpgroups' ds_full for it, i.e. after these loads

@@ -189,7 +189,8 @@ struct BwdLayout {
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
   static constexpr int OFF_STAT = OFF_DO + STAGES * TILE;  // per stage: nl[128], nd[128]
-  static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
+  static constexpr int OFF_EPI = OFF_STAT + STAGES * 1024;   // 2 KB per elementwise warp (epilogue)
+  static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
   // barriers: kv_full, kv_free, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full,
   //           dp_full, ds_full, dkv_done, drain
   static constexpr int NBAR = 2 + 4 * STAGES + 6;
@@ -224,6 +225,42 @@ struct BwdSmem {
   __device__ __forceinline__ uint32_t dkv_done() const { return bar(6 + 4 * STAGES); }
   __device__ __forceinline__ uint32_t drain() const { return bar(7 + 4 * STAGES); }
 };
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Writes a warp's 32 x 32 block of f32 -- lane i holds row i, v its 32 columns --
+// to rows row0 + i (i < rows) of `out` (row stride ld floats), columns [col,
+// col + 32).  Stored straight from the registers, one instruction would touch 32
+// rows 16 bytes each; instead each half-row of 16 columns goes through the warp's
+// 2 KB slice of shared memory `buf` and comes back so that 4 lanes store one row's
+// 64 contiguous bytes (8 rows per instruction).  The 16-byte chunks of a row are
+// rotated by (row / 2) mod 4, so that neither the row-wise writes nor the
+// chunk-wise reads meet a bank twice within a 128-byte wavefront.
+__device__ __forceinline__ void warp_store_rows_f32x32(const uint32_t (&v)[32], uint32_t buf, float* out,
+                                                       size_t row0, size_t ld, int col, int rows) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t wrow = buf + lane * 64;
+  const uint32_t rot = (lane >> 1) & 3;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      st_shared_v4(wrow + ((c ^ rot) << 4), v[16 * hh + 4 * c], v[16 * hh + 4 * c + 1], v[16 * hh + 4 * c + 2],
+                   v[16 * hh + 4 * c + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 8 * i + (lane >> 2), ch = lane & 3;
+      float x[4];
+      ld_shared_v4f(buf + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4), x);
+      if (row < rows)
+        *reinterpret_cast<float4*>(out + (row0 + row) * ld + col + 16 * hh + 4 * ch) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+    __syncwarp();
+  }
+}
 
 // One dK/dV work item: a 128-key tile of one (batch, head), and the range of
 // query tiles that see it (under a causal mask, from the tile holding the key
@@ -617,9 +654,11 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
       if (ok) {
         tc_fence_after();
-        const int key = k0 + r;
-        float* out = (h == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D;
+        const int key0 = k0 + (warp & 3) * 32;  // this warp's first key row
+        const size_t row0 = static_cast<size_t>(bh) * p.Nk + key0;
+        const int rows = min(32, p.Nk - key0);
         const uint32_t col = lane_base + (h == 0 ? L::TM_DV : L::TM_DK);
+        const uint32_t buf = sbase + L::OFF_EPI + (warp - 4) * 2048;
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t v[32];
@@ -631,13 +670,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          if (key < p.Nk) {
-            float4* o4 = reinterpret_cast<float4*>(out + cb * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          }
+          warp_store_rows_f32x32(v, buf, h == 0 ? p.dv : p.dk, row0, D, cb * 32, rows);
         }
         // the next item's first MMA3 / MMA4 overwrite dV and dK only after these
         // warpgroups' p_full for it, i.e. after these loads
