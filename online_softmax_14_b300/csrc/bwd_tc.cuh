@@ -35,7 +35,7 @@
 //       MMA1  S^T_t  = K Q_t^T            (A = K, B = Q_t, both from SMEM)
 //       MMA2  dP^T_t = V dO_t^T           (A = V, B = dO_t)
 //       MMA3  dV    += P^T_t dO_t          (A = P^T from TMEM, B = dO_t MN-major)
-//       MMA4  dK    += dS^T_t Q_t          (A = dS^T from TMEM, B = Q_t MN-major)
+//       MMA4  dK    += dS^T_t Q_t          (A = dS^T from SMEM, B = Q_t MN-major)
 //    issued as MMA3_t, MMA1_{t+1}, MMA4_t, MMA2_{t+1}: each product overwrites a
 //    tensor-memory region only after the product reading it was issued, and the
 //    tensor cores run in issue order.  While the elementwise warps form dS^T_t,
@@ -53,12 +53,20 @@
 //              Thread r owns key row r (TMEM lane r) of S^T and dP^T:
 //                P^T = 2^(S^T scale log2e + nl) with the causal / padding mask,
 //                written back to TMEM as bf16 (aliasing S^T); then
-//                dS^T = P^T (dP^T scale + nd) -> bf16, into TMEM (aliasing dP^T).
+//                dS^T = P^T (dP^T scale + nd) -> bf16, into shared memory.
 //              At the end of an item warpgroup 0 writes dV and warpgroup 1 dK.
+//
+// dS^T goes through shared memory rather than tensor memory: measured on B300,
+// the elementwise warps' tcgen05.st of dS^T slowed the product running beside
+// it (MMA3, whose A operand it reads from tensor memory) more than the shared-
+// memory stores and the extra shared-memory operand of MMA4 cost (3.6 % of the
+// backward).  The same move for P^T gained nothing, and for the dQ kernel's dS
+// it lost 6 %: that kernel's products already read close to the shared
+// memory's bandwidth.
 //
 // Tensor memory (512 columns, f32 unless noted):
 //   [0,128)   S^T_t, then P^T_t (bf16: queries 0-63 in [0,32), 64-127 in [64,96))
-//   [128,256) dP^T_t, then dS^T_t (bf16, laid out like P^T)
+//   [128,256) dP^T_t
 //   [256,384) dV   [384,512) dK
 //
 // Every wait is bounded, as in the forward kernel: a wait that runs out records
@@ -188,15 +196,16 @@ struct BwdLayout {
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
-  static constexpr int OFF_STAT = OFF_DO + STAGES * TILE;  // per stage: nl[128], nd[128]
-  static constexpr int OFF_EPI = OFF_STAT + STAGES * 1024;   // 2 KB per elementwise warp (epilogue)
-  static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
+  static constexpr int OFF_DS = OFF_DO + STAGES * TILE;    // dS^T_t, K-major (MMA4's A); epilogue staging
+  static constexpr int OFF_STAT = OFF_DS + TILE;            // per stage: nl[128], nd[128]
+  static constexpr int OFF_BAR = OFF_STAT + STAGES * 1024;
   // barriers: kv_full, kv_free, q_full[S], do_full[S], q_empty[S], do_empty[S], s_full, p_full,
   //           dp_full, ds_full, dkv_done, drain
   static constexpr int NBAR = 2 + 4 * STAGES + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_MISC + 32 + 1024;  // room to align the base up to 1024 bytes
-  // S^T, then P^T (bf16, in each half's own columns) | dP^T, then dS^T | dV | dK
+  // the dynamic shared memory starts 1024-byte aligned (checked at launch): no slack
+  static constexpr int BYTES = OFF_MISC + 32;
+  // S^T, then P^T (bf16, in each half's own columns) | dP^T | dV | dK
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -228,6 +237,20 @@ struct BwdSmem {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later reads of
+// them by the tensor cores (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// A group of 8 MMAs (K = 128): A K-major in shared memory (two 16 KB column
+// blocks, 32 bytes per step), B MN-major (16 rows = 2 KB per step).
+__device__ __forceinline__ void umma_ss_kmn8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_UMMA_HEAD FA_UMMA_SS_FIRST FA_UMMA_SS(2, 128) FA_UMMA_SS(4, 256) FA_UMMA_SS(6, 384)
+                   FA_UMMA_SS(1024, 512) FA_UMMA_SS(1026, 640) FA_UMMA_SS(1028, 768) FA_UMMA_SS(1030, 896) "}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+               : "memory");
 }
 
 // Writes a warp's 32 x 32 block of f32 -- lane i holds row i, v its 32 columns --
@@ -290,8 +313,13 @@ __global__ void __launch_bounds__(384, 1)
                     const BwdParams p, const __grid_constant__ WorkList sc) {
   using L = BwdLayout<STAGES>;
   constexpr int D = L::D;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the layout fills the shared memory: it needs a 1024-byte aligned base
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, ST_BWD_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* issued_q = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
@@ -428,6 +456,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t d_do = sdesc_sw128(sbase + L::OFF_DO, 16, 1024);
     const uint64_t m_q = sdesc_sw128(sbase + L::OFF_Q, L::COLBLK, 1024);  // MN-major: Q, dO
     const uint64_t m_do = sdesc_sw128(sbase + L::OFF_DO, L::COLBLK, 1024);
+    const uint64_t d_ds = sdesc_sw128(sbase + L::OFF_DS, 16, 1024);  // K-major: dS^T
     constexpr uint32_t TILE16 = L::TILE >> 4;
 
     // S^T = K Q_t^T or dP^T = V dO_t^T: both operands K-major, two column blocks each
@@ -498,7 +527,7 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        mma_grad(tmem + L::TM_DK, tmem + L::TM_DP, m_q + st * TILE16, t == 0);
+        umma_ss_kmn8(tmem + L::TM_DK, d_ds, m_q + st * TILE16, IDESC_G, t == 0 ? 0u : 1u);
         umma_commit_w(sm.q_empty(st));
         // MMA2: dP^T_{t+1} into the dP columns (dS^T_t was read by MMA4_t)
         if (next) {
@@ -538,7 +567,8 @@ __global__ void __launch_bounds__(384, 1)
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + L::TM_S + h * 64;   // this half's S^T, then its P^T
-    const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T, then its dS^T
+    const uint32_t dp_col = lane_base + L::TM_DP + h * 64;  // this half's dP^T
+    const uint32_t ds_row = sbase + L::OFF_DS + h * L::COLBLK + r * 128;  // this key row's dS^T
     const float sl = p.scale_log2, scale = p.scale;
     const uint32_t stat = sbase + L::OFF_STAT + h * 256;  // + stage * 1024: nl; + 512: nd
     bool ok = true;
@@ -639,12 +669,16 @@ __global__ void __launch_bounds__(384, 1)
               dsk[(j4 + w) / 2] = pack_bf16x2(g0, g1);
             }
           }
-          // dS^T as MMA4's A operand: bf16 pairs into the first 32 of this half's
-          // dP columns (dP^T has been read into registers)
-          FA_TMEM_ST32(dp_col, dsk);
-          tmem_wait_st();
+          // dS^T as MMA4's A operand, K-major in shared memory: this half's 64
+          // queries are column block h, key row r is 128 bytes with its 16-byte
+          // chunks rotated by r mod 8 (the 128-byte swizzle).  MMA4_{t-1}, the last
+          // reader of the buffer, ran before dP^T_t was formed.
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
+          fence_proxy_async_smem();
         }
-        tc_fence_before();
+        tc_fence_before();  // the dP^T loads complete before MMA2_{t+1} overwrites the columns
         mbar_arrive(sm.ds_full());
       }
 
@@ -658,7 +692,9 @@ __global__ void __launch_bounds__(384, 1)
         const size_t row0 = static_cast<size_t>(bh) * p.Nk + key0;
         const int rows = min(32, p.Nk - key0);
         const uint32_t col = lane_base + (h == 0 ? L::TM_DV : L::TM_DK);
-        const uint32_t buf = sbase + L::OFF_EPI + (warp - 4) * 2048;
+        // staging: the first 2 KB of this warp's own rows of the dS^T buffer (free:
+        // the item's products have run, and its next dS^T rows come after this)
+        const uint32_t buf = sbase + L::OFF_DS + h * L::COLBLK + (warp & 3) * 4096;
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t v[32];
