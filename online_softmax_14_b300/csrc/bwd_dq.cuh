@@ -480,13 +480,6 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        // ... and once S_{j+1} has run: tcgen05.st beside a product that reads its A
-        // operand from tensor memory slows that product (measured: 1.7 % of the
-        // backward); dP_{j+1}, which runs next, takes both operands from SMEM
-        if (!__all_sync(0xffffffffu, j + 1 >= n || mbar_wait(sm.s_full(), (G + 1) & 1, wc, ST_BWD_TIMEOUT_S))) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
         FA_TMEM_ST32(lane_base + L::TM_DS + h * 32, dsk);
         tmem_wait_st();
