@@ -672,13 +672,7 @@ __global__ void __launch_bounds__(384, 1)
           // dS^T as MMA4's A operand, K-major in shared memory: this half's 64
           // queries are column block h, key row r is 128 bytes with its 16-byte
           // chunks rotated by r mod 8 (the 128-byte swizzle).  MMA4_{t-1}, the last
-          // reader of the buffer, ran before dP^T_t was formed.  The stores wait for
-          // MMA3_t (do_empty of the stage), which they would otherwise slow down:
-          // measured 1.5 % faster over the backward.
-          if (!__all_sync(0xffffffffu, mbar_wait(sm.do_empty(st), (T / STAGES) & 1, wc, ST_BWD_TIMEOUT_DS))) {
-            ok = false;
-            break;
-          }
+          // reader of the buffer, ran before dP^T_t was formed.
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
