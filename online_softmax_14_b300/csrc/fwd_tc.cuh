@@ -118,7 +118,8 @@ struct TcLayout {
   static constexpr int TILE = BM * D * 2;     // bytes of a Q, K or V tile
   static constexpr int OFF_Q = 0;             // Q0, Q1
   static constexpr int OFF_KV = 2 * TILE;     // NS slots
-  static constexpr int OFF_BAR = OFF_KV + NS * TILE;
+  static constexpr int OFF_EPI = OFF_KV + NS * TILE;  // 2 KB per softmax warp (O epilogue)
+  static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
   // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
   static constexpr int NBAR = 2 + 2 * NS + 6 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -127,6 +128,37 @@ struct TcLayout {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(BYTES <= 232448, "shared memory budget");
 };
+
+// Writes a warp's 32 rows x 32 bf16 -- lane i holds row i as 16 packed pairs --
+// to rows row0 + i (i < rows) of `out` (row stride ld elements), columns [col,
+// col + 32).  Stored straight from the registers, one instruction would touch 32
+// rows 16 bytes each, at half the SM's store rate; through the warp's 2 KB slice
+// of shared memory `buf` they come back so that 4 lanes store one row's 64
+// contiguous bytes.  The 16-byte chunks of a row are rotated by (row / 2) mod 4,
+// so that neither the row-wise writes nor the chunk-wise reads meet a bank twice
+// within a 128-byte wavefront.
+__device__ __forceinline__ void warp_store_rows_bf16x32(const uint32_t (&w)[16], uint32_t buf, __nv_bfloat16* out,
+                                                        size_t row0, size_t ld, int col, int rows) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t rot = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + ((c ^ rot) << 4)), "r"(w[4 * c]),
+                 "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                 : "memory");
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 8 * i + (lane >> 2), ch = lane & 3;
+    uint4 x;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                 : "r"(buf + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4))
+                 : "memory");
+    if (row < rows) *reinterpret_cast<uint4*>(out + (row0 + row) * ld + col + 8 * ch) = x;
+  }
+  __syncwarp();
+}
 
 // Shared-memory addresses (32-bit) of the forward kernel's buffers and
 // barriers, from the 1024-aligned base of its dynamic shared memory.  Each
@@ -537,7 +569,9 @@ __global__ void __launch_bounds__(384, 1)
       if (ok && qt0c - p.qoff < p.N) {
         tc_fence_after();
         const float inv = (l > 0.f) ? 1.f / (l + dl) : 0.f;  // guard: l = 0 -> zero vector
-        const size_t orow = (static_cast<size_t>(bh) * p.N + qrow) * D;
+        const int qr0 = qt0c - p.qoff + (warp & 3) * 32;  // this warp's first row
+        const int rows = min(32, p.N - qr0);
+        const uint32_t buf = sm.base + L::OFF_EPI + warp * 2048;
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t orr[32];
@@ -553,11 +587,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             ob[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
-          if (qrow < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + orow + cb * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
-          }
+          warp_store_rows_bf16x32(ob, buf, p.o, static_cast<size_t>(bh) * p.N + qr0, D, cb * 32, rows);
         }
         if (p.lse && qrow < p.N)
           p.lse[static_cast<size_t>(bh) * p.N + qrow] = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
