@@ -120,11 +120,17 @@ struct TcLayout {
   static constexpr int OFF_KV = 2 * TILE;     // NS slots
   static constexpr int OFF_EPI = OFF_KV + NS * TILE;  // 2 KB per softmax warp (O epilogue)
   static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
-  // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 2 + 2 * NS + 6 + 1;
+  // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain,
+  //           s_free[2], pv_done[2] (separate-P layout only)
+  static constexpr int NBAR = 2 + 2 * NS + 6 + 1 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D, TM_COLS = 512;
+  // At d = 64, P_i gets columns of its own ([384, 448), [448, 512)) instead of
+  // aliasing S_i: S_i(j+1) can then be formed while the softmax still turns
+  // S_i(j) into P_i(j).  At d = 128 the accumulators leave no room.
+  static constexpr bool SEP_P = D == 64;
+  static constexpr uint32_t TM_P0 = SEP_P ? 384 : TM_S0, TM_P1 = SEP_P ? 448 : TM_S1;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -179,6 +185,10 @@ struct FwdSmem {
   __device__ __forceinline__ uint32_t p_full(int t) const { return bar(4 + 2 * NS + t); }
   __device__ __forceinline__ uint32_t o_done(int t) const { return bar(6 + 2 * NS + t); }
   __device__ __forceinline__ uint32_t drain() const { return bar(8 + 2 * NS); }
+  // separate-P layout: the softmax has read S_t (one phase per block)
+  __device__ __forceinline__ uint32_t s_free(int t) const { return bar(9 + 2 * NS + t); }
+  // separate-P layout: P_t V has run, so P_t and O_t may be written (one phase per block)
+  __device__ __forceinline__ uint32_t pv_done(int t) const { return bar(11 + 2 * NS + t); }
 };
 
 // One item's geometry, computed alike by every role.
@@ -242,6 +252,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(sm.s_full(i), 1);
       mbar_init(sm.p_full(i), 128);
       mbar_init(sm.o_done(i), 1);
+      mbar_init(sm.s_free(i), 128);
+      mbar_init(sm.pv_done(i), 1);
     }
     mbar_init(sm.drain(), 1);
     *abort_flag = 0;
@@ -358,6 +370,7 @@ __global__ void __launch_bounds__(384, 1)
     };
     const uint32_t tS0 = tmem + L::TM_S0, tS1 = tmem + L::TM_S1;
     const uint32_t tO0 = tmem + L::TM_O0, tO1 = tmem + L::TM_O1;
+    const uint32_t tP0 = tmem + L::TM_P0, tP1 = tmem + L::TM_P1;
 
     int c = 0, nq = 0;    // K/V loads consumed, items started
     int jb0 = 0, jb1 = 0; // blocks of each query tile done in earlier items (s_full / p_full phases)
@@ -370,6 +383,13 @@ __global__ void __launch_bounds__(384, 1)
       ++nq;
       if (!ok) break;
       tc_fence_after();
+      if constexpr (L::SEP_P) {
+        // S_i of the item's first block reuses columns the softmax read last
+        ok = (n_t0 == 0 || jb0 == 0 || mbar_wait_w(sm.s_free(0), (jb0 - 1) & 1, wc, ST_TIMEOUT_S)) &&
+             (n_t1 == 0 || jb1 == 0 || mbar_wait_w(sm.s_free(1), (jb1 - 1) & 1, wc, ST_TIMEOUT_S));
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (n_t0 > 0) issue_s(tS0, 0, sm.s_full(0), c);
       if (n_t1 > 0) issue_s(tS1, L::TILE, sm.s_full(1), c);
       umma_commit_w(sm.kv_empty(c % NS));
@@ -390,6 +410,48 @@ __global__ void __launch_bounds__(384, 1)
           if (k1_ready) tc_fence_after();
           return k1_ready;
         };
+        if constexpr (L::SEP_P) {
+          // S0_{j+1} and S1_{j+1} as soon as the softmax has read S0_j, S1_j; then
+          // PV0_j and PV1_j (P in columns of its own), each committing pv_done
+          if (j1 < n_t0) {
+            if (!mbar_wait_w(sm.s_free(0), (jb0 + j) & 1, wc, ST_TIMEOUT_S) || !wait_k1()) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(tS0, 0, sm.s_full(0), ck);
+          }
+          if (j1 < n_t1) {
+            if (!mbar_wait_w(sm.s_free(1), (jb1 + j) & 1, wc, ST_TIMEOUT_S) || !wait_k1()) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(tS1, L::TILE, sm.s_full(1), ck);
+          }
+          if (j < n_t0) {
+            if (!wait_v() || !mbar_wait_w(sm.p_full(0), (jb0 + j) & 1, wc, ST_TIMEOUT_P)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(tO0, tP0, sm.o_done(0), cv, j == 0, j + 1 == n_t0);
+            umma_commit_w(sm.pv_done(0));
+          }
+          if (j < n_t1) {
+            if (!wait_v() || !mbar_wait_w(sm.p_full(1), (jb1 + j) & 1, wc, ST_TIMEOUT_P)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(tO1, tP1, sm.o_done(1), cv, j == 0, j + 1 == n_t1);
+            umma_commit_w(sm.pv_done(1));
+          }
+          umma_commit_w(sm.kv_empty(cv % NS));
+          if (j1 < n_max) umma_commit_w(sm.kv_empty(ck % NS));
+          if (j1 == n_max - 1) umma_commit_w(sm.q_empty());
+          continue;
+        }
         // tile 0: PV0_j, then S0_{j+1}
         if (j < n_t0) {
           if (!wait_v() || !mbar_wait_w(sm.p_full(0), (jb0 + j) & 1, wc, ST_TIMEOUT_P)) {
@@ -448,6 +510,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r = threadIdx.x & 127;   // row in the tile == tensor-memory lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + (ti ? L::TM_S1 : L::TM_S0);
+    const uint32_t p_col = lane_base + (ti ? L::TM_P1 : L::TM_P0);  // = s_col unless SEP_P
     const uint32_t o_col = lane_base + (ti ? L::TM_O1 : L::TM_O0);
     const float sl = p.scale_log2;
     int jb = 0, no = 0;  // blocks of this tile done in earlier items; items that signalled o_done
@@ -480,6 +543,10 @@ __global__ void __launch_bounds__(384, 1)
         FA_REG_FENCE32(sr + 32);
         FA_REG_FENCE32(sr + 64);
         FA_REG_FENCE32(sr + 96);
+        if constexpr (L::SEP_P) {
+          tc_fence_before();
+          mbar_arrive(sm.s_free(ti));  // S_(j+1) may overwrite the scores now
+        }
 
         const int k0 = j * L::BN;
         // causal: key k visible iff k < row + qoff
@@ -514,6 +581,15 @@ __global__ void __launch_bounds__(384, 1)
         // x = s * scale*log2(e) - m_ref two scores at a time (f32x2), p = 2^x, row
         // sum in 4 independent chains; P in quarters of 32 scores (16 packed
         // columns) keeps register use low
+        if constexpr (L::SEP_P) {
+          // P_j and the accumulator's rescale wait for P V of the previous block
+          // (with S_j formed ahead of it, s_full no longer implies it has run)
+          if (jb + j > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.pv_done(ti), (jb + j - 1) & 1, wc, ST_TIMEOUT_P))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_ref, -m_ref);
         // row sum in two f32x2 chains: one packed add per pair of scores
         uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
@@ -537,7 +613,7 @@ __global__ void __launch_bounds__(384, 1)
             f2_unpack(p2, p0, p1);
             pk[i] = pack_bf16x2(p0, p1);
           }
-          FA_TMEM_ST16(s_col + 16 * h, pk);
+          FA_TMEM_ST16(p_col + 16 * h, pk);
         }
         float ra, rb, rc, rd;
         f2_unpack(rs2[0], ra, rb);
@@ -545,7 +621,8 @@ __global__ void __launch_bounds__(384, 1)
         l = l * c + ((ra + rb) + (rc + rd));
         if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
           // The accumulator already holds blocks < j: PV_{j-1} was issued before
-          // S_j, and s_full for S_j tracks every earlier tensor-core operation.
+          // S_j, and s_full for S_j tracks every earlier tensor-core operation
+          // (separate-P layout: the pv_done wait above).
 #pragma unroll
           for (int cb = 0; cb < D / 32; ++cb) {
             uint32_t orr[32];
