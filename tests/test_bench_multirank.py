@@ -104,3 +104,16 @@ def test_forward_source_digest_covers_kernel_and_launch_only():
     lib = open(os.path.join(ROOT, "online_softmax_14_b300", "csrc", "fa_lib.cu"), encoding="utf-8").read()
     for head in bench.FWD_HOST_FUNCTIONS:
         assert bench._function_text(lib, head).startswith(head)
+
+
+def test_recorded_forward_traffic_matches_the_current_sources():
+    """The DRAM traffic bench.py reports for the headline workload was captured
+    with ncu on the forward sources as they are now: a change to the forward's
+    headers or launch code without a new capture fails here rather than
+    silently turning the reported traffic into null."""
+    import bench
+
+    rec = bench.NCU_TRAFFIC["bf16_causal_B2_H32_N8192_d128"]
+    assert rec["src_digest"] == bench.kernel_src_digest()
+    # the algorithmic bytes of that workload are 539 MB; the capture is within 10 %
+    assert 539e6 <= rec["bytes"] <= 1.1 * 539e6
